@@ -1,0 +1,359 @@
+"""Benchmark of the paged decode step (KV write + decode attention) at Llama-3-8B GQA shapes.
+
+One step = one layer's pass of the hot path over the serving batch: ``paged_kv_write`` of the 64
+new tokens through ``slot_mapping``, then ``paged_attention_decode`` (split-K partitions and the
+log-sum-exp merge included) — 32 query / 8 KV heads, head_dim 128, block_size 16, bf16, batch 64,
+context lengths uniform in [512, 4096], block tables drawn from a shuffled 40,000-block pool.
+
+Timed on the device with CUDA events after warm-up; steps rotate over several independent layer
+pools so that no step finds its K/V in L2 (each step reads ~604 MB; the rotation spans > 2 GB).
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attn: KV GB/s (% HBM roofline) and decode tok/s, Llama-3-8B GQA"
+UNIT = "GB/s"
+HQ, HKV, D, S = 32, 8, 128, 16
+LLAMA_LAYERS = 32
+ELT = 2  # bf16
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def algorithmic_bytes(lens, batch):
+    """Bytes the step must move at minimum: K and V of exactly context_len tokens per sequence and
+    KV head, the queries and outputs, the table entries and lengths read, and the write (new K/V
+    read once, written once, plus slots)."""
+    kv = sum(lens) * HKV * D * ELT * 2
+    qo = 2 * batch * HQ * D * ELT
+    tables = sum(W.ceil_div(n, S) for n in lens) * 4 + batch * 4
+    write = batch * HKV * D * ELT * 2 * 2 + batch * 8
+    return kv + qo + tables, write
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (clocks and throttle reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return rank, world, local, dist
+    if n_gpus > 1:
+        print(json.dumps({"warning": "--gpus > 1 without torchrun; running one replica"}), file=sys.stderr)
+    return 0, 1, 0, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(budget_s: float = 12.0, max_seqs: int = 16):
+    """The oracle (fp64 numpy, gather + explicit repeat + two-pass softmax), as it stands, on the
+    host cores, over the first sequences of the same serving batch until the budget is spent."""
+    import oracle
+    lens = W.llama_context_lens()
+    done_bytes, spent, seqs = 0, 0.0, 0
+    while seqs < max_seqs and spent < budget_s:
+        n = lens[seqs]
+        case = W.decode_case("cpu_sample", W.SEED_BASE + 3 + 17 * seqs, [n - 1], n_q_heads=HQ, n_kv_heads=HKV,
+                             head_dim=D, block_size=S, dtype=torch.bfloat16,
+                             num_blocks=W.ceil_div(n, S) + 1, max_blocks_per_seq=W.LLAMA_MAX_CTX // S)
+        t0 = time.perf_counter()
+        kp, vp = oracle.paged_kv_write(case.k_pool, case.v_pool, case.k_new, case.v_new, case.slot_mapping)
+        oracle.paged_decode(case.q, kp, vp, case.block_table, case.context_lens, case.scale)
+        spent += time.perf_counter() - t0
+        kvb, wb = algorithmic_bytes([n], 1)
+        done_bytes += kvb + wb
+        seqs += 1
+    return {"value": done_bytes / spent / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {seqs} of the 64 serving sequences (write + decode, {sum(lens[:seqs])} tokens), "
+                      f"{spent:.1f} s of single-threaded numpy"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    lens = W.llama_context_lens()
+    # one bounded sample per step: two sequences of the serving batch (rotating)
+    cases = []
+    for i in range(4):
+        sel = [lens[(2 * i) % 64], lens[(2 * i + 1) % 64]]
+        cases.append((sel, W.decode_case("ref_sample", W.SEED_BASE + 3 + i, [n - 1 for n in sel], n_q_heads=HQ,
+                                         n_kv_heads=HKV, head_dim=D, block_size=S, dtype=torch.bfloat16,
+                                         num_blocks=sum(W.ceil_div(n, S) for n in sel) + 2,
+                                         max_blocks_per_seq=W.LLAMA_MAX_CTX // S)))
+
+    def step(i):
+        sel, c = cases[i % len(cases)]
+        kp, vp = oracle.paged_kv_write(c.k_pool, c.v_pool, c.k_new, c.v_new, c.slot_mapping)
+        oracle.paged_decode(c.q, kp, vp, c.block_table, c.context_lens, c.scale)
+        kvb, wb = algorithmic_bytes(sel, len(sel))
+        return kvb + wb
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    total = 0
+    for i in range(args.steps):
+        total += step(i)
+    dt = time.perf_counter() - t0
+    value = total / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) K/V/Q, bf16-cast, upcast to fp64)",
+            "config": {"workload": "llama3_8b_serving_decode sample: 2 sequences of the batch-64 "
+                                   "U[512,4096] serving step per step", "heads": "32q/8kv", "head_dim": D,
+                       "block_size": S},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "2 of the 64 serving sequences per step (write + decode)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=4, help="independent layer pools rotated over the steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    rank, world, local, dist = dist_setup(args.gpus)
+    import pagedattention_kv_cache_paged_gb300 as pa
+    lib = pa.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    lens = W.llama_context_lens()
+    B = len(lens)
+    inp = W.device_decode_inputs(lens, n_q_heads=HQ, n_kv_heads=HKV, head_dim=D, block_size=S,
+                                 dtype=torch.bfloat16, num_blocks=W.LLAMA_POOL,
+                                 max_blocks_per_seq=W.LLAMA_MAX_CTX // S, device=dev,
+                                 seed=W.SEED_BASE + 3 + 1000 * rank, layers=args.layers)
+    table = inp["block_table"].to(dev)
+    ctx = inp["context_lens"].to(dev)
+    slot = inp["slot_mapping"].to(dev)
+    q = inp["q"].to(dev)
+    kn, vn = inp["k_new"].to(dev), inp["v_new"].to(dev)
+    out = torch.empty_like(q)
+    bt_stride = table.stride(0)
+    ws_bytes = pa.decode_workspace_size(B, bt_stride, S, HQ, HKV, D)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(D)
+    pools = inp["pools"]
+    ptr = {k: v.data_ptr() for k, v in dict(table=table, ctx=ctx, slot=slot, q=q, kn=kn, vn=vn, out=out,
+                                            ws=ws).items()}
+
+    def write(layer):
+        kp, vp = pools[layer]
+        st = lib.paged_kv_write(ptr["kn"], ptr["vn"], ptr["slot"], B, kp.data_ptr(), vp.data_ptr(),
+                                W.LLAMA_POOL, S, HKV, D, pa.PA_BF16, sp)
+        if st:
+            raise RuntimeError(f"paged_kv_write status {st}")
+
+    def decode(layer):
+        kp, vp = pools[layer]
+        st = lib.paged_attention_decode(ptr["out"], ptr["q"], kp.data_ptr(), vp.data_ptr(), ptr["table"],
+                                        bt_stride, ptr["ctx"], B, W.LLAMA_POOL, S, scale, HQ, HKV, D,
+                                        pa.PA_BF16, ptr["ws"], ws_bytes, sp)
+        if st:
+            raise RuntimeError(f"paged_attention_decode status {st}")
+
+    for i in range(args.warmup):
+        write(i % args.layers)
+        decode(i % args.layers)
+    K = args.steps
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(dist)
+    launches0 = pa.launch_count()
+    clocks.start()
+    ev0.record(stream)
+    for i in range(K):
+        layer = i % args.layers
+        write(layer)
+        ev_dec[i][0].record(stream)
+        decode(layer)
+        ev_dec[i][1].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(dist)
+    launches = pa.launch_count() - launches0
+    total_ms = max_over_ranks(ev0.elapsed_time(ev1), dist)
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_dec)
+    kvb, wb = algorithmic_bytes(lens, B)
+    step_bytes = kvb + wb
+    ms_per_step = total_ms / K
+    value = step_bytes * K * world / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = kvb / (dec_ms * 1e-3) / 1e9
+    if pa.device_error_flags() != 0:
+        raise RuntimeError("device error word set during the benchmark")
+
+    # end to end through the C ABI with pinned host buffers: inputs in, output out, every step
+    e2e = None
+    E = args.e2e_steps
+    if E > 0:
+        host = {k: t.cpu().pin_memory() for k, t in dict(q=q, kn=kn, vn=vn, slot=slot, table=table, ctx=ctx).items()}
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = host_out.numel() * host_out.element_size()
+        devs = dict(q=q, kn=kn, vn=vn, slot=slot, table=table, ctx=ctx)
+
+        def e2e_step(i):
+            for k in host:
+                devs[k].copy_(host[k], non_blocking=True)
+            write(i % args.layers)
+            decode(i % args.layers)
+            host_out.copy_(out, non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(E):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), dist)
+        e2e = {"value": step_bytes * E * world / (e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / E}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V, bf16)",
+        "config": {"workload": "llama3_8b_serving_decode: paged_kv_write of 64 tokens + paged decode attention, "
+                               "32q/8kv heads, head_dim 128, block_size 16, batch 64, context U[512,4096], "
+                               "40,000-block shuffled pool",
+                   "context_tokens": sum(lens), "batch": B,
+                   "l2": f"inputs larger than L2: {args.layers} rotating layer pools, "
+                         f"{kvb / 1e6:.0f} MB of K/V read per step",
+                   "parallelism": f"replicas x{world}"},
+        "pct_hbm_measured": value / peak,
+        "pct_hbm_spec_8000": value / 8000.0,
+        "decode_tok_s_attention_only": B * world / (LLAMA_LAYERS * ms_per_step * 1e-3),
+        "kernel_us": {"decode_call": dec_ms * 1e3, "step": ms_per_step * 1e3},
+        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (partition + merge kernels)",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,200 @@
+/*
+ * pagedattn.h — C ABI of the paged KV-cache attention library (libpagedattn.so).
+ *
+ * The library implements the device hot path of PagedAttention over a block-table-indexed KV cache
+ * on one GPU (sm_103a): the slot-mapped K/V write, decode attention straight from scattered
+ * physical blocks (read-time GQA, single-pass online softmax, split-K with an exact log-sum-exp
+ * merge), causal chunked prefill over a paged history, and the block copy used by copy-on-write
+ * forks.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory.  Every pointer argument is a DEVICE pointer unless stated otherwise.  The caller owns all
+ *   buffers (pools, tables, outputs, workspace); the library allocates nothing and frees nothing.
+ *   Each call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *   stream) and returns after enqueueing its kernels.
+ * Pools.  A K pool and a V pool are each a contiguous array [num_blocks][block_size][n_kv_heads]
+ *   [head_dim] of the I/O dtype (Pico-vLLM dev log #5 "Paged Attention", core data structures:
+ *   the device cache tensor is indexed block, token-in-block, kv head, head dim; JuliaPagedAttn
+ *   README, "Block Layout": a block holds block_size consecutive tokens for every KV head).
+ *   Pool base pointers must be 16-byte aligned.
+ * Slots.  Logical position j of sequence b lives in slot
+ *   block_table[b * block_table_stride + j / block_size] * block_size + j % block_size,
+ *   i.e. row `slot` of the pool viewed as [num_blocks * block_size][n_kv_heads][head_dim].
+ * Tables.  block_table is int32 [batch][block_table_stride] (Pico-vLLM dev log #5,
+ *   get_block_table: int32 physical ids); entries past ceil(context_lens[b] / block_size) are never
+ *   read.  context_lens is int32 [batch] and counts the token(s) just written (Pico-vLLM dev log
+ *   #5: the current token's K/V already exist in every layer, hence the +1 correction).
+ * GQA.  n_q_heads must be a multiple of n_kv_heads; query head i reads KV head
+ *   i / (n_q_heads / n_kv_heads).  The cache stores only the KV heads and the repeat happens at
+ *   read time (nanoserve "Day 19: the fused paged read wired into attention", "What I learned" 4).
+ * Dtypes.  q, pools and out share one dtype (PA_BF16, PA_FP16 or PA_FP32); scores, softmax
+ *   statistics and accumulators are fp32; outputs are rounded to nearest-even.
+ * Supported shapes.  head_dim in {64, 128}; block_size a power of two in [1, 256];
+ *   n_q_heads / n_kv_heads in {1, 2, 4, 8}.  Other shapes return PA_EUNSUPPORTED.
+ * Errors.  0 = success.  Negative values (PA_E*) mean nothing was launched, except PA_ECUDA,
+ *   which reports a launch failure (pa_last_cuda_error() gives the cudaError_t).  Device code never
+ *   traps: an out-of-range block id, slot or copy pair met on the device is skipped (treated as
+ *   masked) and recorded in a device error word that pa_device_error_flags() reads back.  With
+ *   checked mode on (pa_set_option(PA_OPT_CHECKED, 1)) each call first copies its index arrays to
+ *   the host, synchronizing `stream`, and returns PA_ERANGE without launching if any index, length
+ *   or duplicate is invalid.
+ */
+#ifndef PAGEDATTN_H_
+#define PAGEDATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_BF16 = 0, PA_FP16 = 1, PA_FP32 = 2 } pa_dtype;
+
+enum {
+  PA_OK = 0,
+  PA_EINVAL = -1,        /* null pointer, negative or inconsistent size, heads not divisible */
+  PA_EDTYPE = -2,        /* dtype not one of pa_dtype */
+  PA_ERANGE = -3,        /* checked mode: block id / slot / length / pair out of range or duplicate */
+  PA_EWORKSPACE = -4,    /* workspace given but smaller than required or not 16-byte aligned */
+  PA_ECUDA = -5,         /* a CUDA launch failed; see pa_last_cuda_error() */
+  PA_EUNSUPPORTED = -6   /* shape outside the supported set (see "Supported shapes") */
+};
+
+/* Bits of the device error word (pa_device_error_flags). */
+enum {
+  PA_DEVERR_BLOCK_ID = 1,     /* a table entry inside a context was < 0 or >= num_blocks */
+  PA_DEVERR_SLOT = 2,         /* a slot >= num_blocks * block_size */
+  PA_DEVERR_CONTEXT_LEN = 4,  /* context_lens[b] < 0 or > block_table_stride * block_size */
+  PA_DEVERR_COPY_PAIR = 8,    /* a copy pair with src or dst outside [0, num_blocks) */
+  PA_DEVERR_QUERY_LOC = 16,   /* query_start_loc not non-decreasing, or a chunk longer than its context */
+  PA_DEVERR_TIMEOUT = 32      /* a bounded wait in a pipelined kernel gave up (the kernel returned early) */
+};
+
+/* Options for pa_set_option / pa_get_option (process-wide). */
+enum {
+  PA_OPT_CHECKED = 1,          /* 0 (default) or 1: host-side validation before each launch */
+  PA_OPT_DECODE_KERNEL = 2,    /* 0 auto (default), 1 CUDA-core kernel, 2 tensor-core kernel */
+  PA_OPT_PARTITION_TOKENS = 3, /* 0 auto (default) or split-K partition length in tokens (>= block_size) */
+  PA_OPT_PREFILL_KERNEL = 4    /* 0 auto (default), 1 CUDA-core kernel, 2 tensor-core kernel */
+};
+
+/*
+ * paged_kv_write — scatter this step's K/V into the pools through slot_mapping.
+ * Source: nanoserve Day 19, "What I learned" 2 (the shared write scatters the K/V to this step's
+ * slots) and "Diagram" (the write goes through slot_mapping); JuliaPagedAttn README, API
+ * "write_kv_cache!".
+ *   k_new, v_new   [n_tokens][n_kv_heads][head_dim], dtype, contiguous (read only)
+ *   slot_mapping   int64 [n_tokens]; token t is written to pool row slot_mapping[t]; a negative
+ *                  slot writes nothing for that token.  Slots must be distinct (duplicates race;
+ *                  checked mode rejects them).
+ *   k_pool, v_pool pools as above (written in place).  The copy is bit-exact.
+ * n_tokens == 0 is a no-op returning PA_OK.
+ */
+PA_API int paged_kv_write(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens,
+                   void* k_pool, void* v_pool, int64_t num_blocks, int block_size, int n_kv_heads,
+                   int head_dim, pa_dtype dtype, void* stream);
+
+/*
+ * paged_attention_decode — one query token per sequence attends over its whole paged context.
+ * Source: JuliaPagedAttn README, API "paged_attention_cpu!(O, Q, K_cache, V_cache, block_table,
+ * context_lengths, layer, scale)" and "Online Softmax"; nanoserve Day 19 "What I added today"
+ * (paged_attention(layer, k, v, q, n_rep, scale)).
+ *   out            [batch][n_q_heads][head_dim], dtype (written)
+ *   q              [batch][n_q_heads][head_dim], dtype
+ *   block_table    int32 [batch][block_table_stride]; context_lens int32 [batch]
+ *   scale          multiplies q.k (callers usually pass 1/sqrt(head_dim))
+ *   out[b][i] = sum_j softmax_j(scale * q[b][i] . K_j) V_j over the context_lens[b] tokens of
+ *   sequence b, reading KV head i / (n_q_heads / n_kv_heads).  An empty context gives zeros.
+ *   workspace      optional fp32 scratch for split-K (long contexts are cut into partitions whose
+ *                  partial softmax states are merged exactly by log-sum-exp).  Pass at least
+ *                  paged_attention_decode_workspace_size(...) bytes, 16-byte aligned.  With
+ *                  workspace == NULL every (sequence, KV head) runs as one partition (correct, but
+ *                  slower for long or uneven contexts).  The contents need no initialisation.
+ */
+PA_API int paged_attention_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_table, int64_t block_table_stride,
+                           const int32_t* context_lens, int batch, int64_t num_blocks, int block_size,
+                           float scale, int n_q_heads, int n_kv_heads, int head_dim, pa_dtype dtype,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes paged_attention_decode needs for split-K with these sizes (0 if it never splits). */
+PA_API size_t paged_attention_decode_workspace_size(int batch, int64_t block_table_stride, int block_size,
+                                             int n_q_heads, int n_kv_heads, int head_dim);
+
+/*
+ * paged_attention_prefill — causal chunked prefill over a paged history.
+ * Source: JuliaPagedAttn README, "Features" (batched prefill: all prompt positions in one kernel
+ * call) and API "prefill!".
+ *   q, out          [total_q][n_q_heads][head_dim], dtype
+ *   query_start_loc int32 [batch + 1], non-decreasing, query_start_loc[0] = 0,
+ *                   query_start_loc[batch] = total_q.  Sequence b owns the m_b = qsl[b+1] - qsl[b]
+ *                   queries qsl[b] .. qsl[b+1]-1; an empty chunk (m_b = 0) is allowed.
+ *   context_lens    int32 [batch], history + chunk (the chunk's K/V must already be written).
+ *   The chunk occupies the last m_b positions of the context; its query r (0-based) attends to
+ *   positions 0 .. context_lens[b] - m_b + r inclusive.
+ */
+PA_API int paged_attention_prefill(void* out, const void* q, const int32_t* query_start_loc, int64_t total_q,
+                            const void* k_pool, const void* v_pool, const int32_t* block_table,
+                            int64_t block_table_stride, const int32_t* context_lens, int batch,
+                            int64_t num_blocks, int block_size, float scale, int n_q_heads,
+                            int n_kv_heads, int head_dim, pa_dtype dtype, void* stream);
+
+/*
+ * copy_blocks — make physical block dst a bit copy of block src, in both pools, for each pair.
+ * Source: JuliaPagedAttn README, "Copy-on-Write" (allocate a new block, copy the data, update the
+ * table, decrement the refcount; the table update and refcount stay with the caller) and API
+ * "cow_fork!".
+ *   block_pairs  int64 [n_pairs][2] = (src, dst).  A dst must not appear twice nor as a src of
+ *                another pair (checked mode rejects both); block_bytes = block_size * n_kv_heads *
+ *                head_dim * element size, a multiple of 16.
+ */
+PA_API int copy_blocks(void* k_pool, void* v_pool, const int64_t* block_pairs, int64_t n_pairs,
+                int64_t num_blocks, int64_t block_bytes, void* stream);
+
+/*
+ * paged_attention_lse_merge — merge split-K partials exactly (the partition-combining identity of
+ * the online softmax in JuliaPagedAttn README "Online Softmax", applied to whole partitions).
+ *   part_max   fp32 [rows][n_parts]   running maxima in the log2 domain (score * log2(e))
+ *   part_sum   fp32 [rows][n_parts]   sums of 2^(s - max)
+ *   part_acc   fp32 [rows][n_parts][head_dim]  unnormalised accumulators
+ *   out        [rows][head_dim], dtype: sum_p acc_p 2^(m_p - M) / sum_p l_p 2^(m_p - M), M = max_p m_p;
+ *              partitions with part_sum == 0 are skipped; a row with none left gives zeros.
+ */
+PA_API int paged_attention_lse_merge(void* out, const float* part_max, const float* part_sum,
+                              const float* part_acc, int64_t rows, int n_parts, int head_dim,
+                              pa_dtype dtype, void* stream);
+
+/* Set / get a process-wide option (PA_OPT_*).  pa_set_option returns PA_EINVAL for an unknown option
+ * or a bad value. */
+PA_API int pa_set_option(int option, int64_t value);
+PA_API int64_t pa_get_option(int option);
+
+/* The cudaError_t of the last PA_ECUDA on this thread (0 if none). */
+PA_API int pa_last_cuda_error(void);
+
+/* Short static description of a status code. */
+PA_API const char* pa_status_string(int status);
+
+/* Read (and, if clear != 0, reset) the device error word of the current device.  Synchronizes
+ * `stream`.  Returns the PA_DEVERR_* bits, or a negative status on a CUDA failure. */
+PA_API int pa_device_error_flags(int clear, void* stream);
+
+/* Number of kernels this library has launched in this process (all devices). */
+PA_API uint64_t pa_launch_count(void);
+
+/* Library version string. */
+PA_API const char* pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H_ */

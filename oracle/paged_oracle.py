@@ -84,20 +84,22 @@ def history_slots(table_row, n: int, block_size: int) -> list:
     return [slot_of(table_row, j, block_size) for j in range(n)]
 
 
-def gather_history(pool, table_row, n: int, block_size: int) -> np.ndarray:
+def gather_history(pool, table_row, n: int, block_size: int, kv_head=None) -> np.ndarray:
     """The contiguous ``[n, Hkv, D]`` float64 history of one sequence, read through its block table
-    (nanoserve Day 19 "Why it matters": the gather path)."""
+    (nanoserve Day 19 "Why it matters": the gather path).  With ``kv_head`` set, only that head is
+    gathered and the result is ``[n, 1, D]``."""
     NB, S, Hkv, D = pool.shape
     assert S == block_size
     slots = history_slots(to_int(table_row), n, block_size)
+    heads = slice(None) if kv_head is None else slice(kv_head, kv_head + 1)
     if n == 0:
-        return np.zeros((0, Hkv, D))
+        return np.zeros((0, Hkv if kv_head is None else 1, D))
     if _is_torch(pool):
         flat = pool.reshape(NB * S, Hkv, D)
-        rows = flat[torch.as_tensor(slots, dtype=torch.int64)]
+        rows = flat[torch.as_tensor(slots, dtype=torch.int64)][:, heads]
         return rows.to(torch.float64).numpy()
     flat = np.asarray(pool).reshape(NB * S, Hkv, D)
-    return flat[slots].astype(np.float64)
+    return flat[slots][:, heads].astype(np.float64)
 
 
 def repeat_kv(x: np.ndarray, n_rep: int) -> np.ndarray:
@@ -222,8 +224,8 @@ def paged_decode_rows(q, k_pool, v_pool, block_table, context_lens, scale: float
     res = {}
     for b, kvh in rows:
         n = int(lens[b])
-        kc = gather_history(k_pool, table[b], n, S)[:, kvh:kvh + 1]
-        vc = gather_history(v_pool, table[b], n, S)[:, kvh:kvh + 1]
+        kc = gather_history(k_pool, table[b], n, S, kv_head=kvh)
+        vc = gather_history(v_pool, table[b], n, S, kv_head=kvh)
         res[(b, kvh)] = softmax_attention(qf[b, kvh * g:(kvh + 1) * g], repeat_kv(kc, g),
                                           repeat_kv(vc, g), scale)
     return res

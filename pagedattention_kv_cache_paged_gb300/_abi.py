@@ -1,0 +1,272 @@
+"""ctypes binding of libpagedattn.so: argument marshalling only.
+
+Every function here checks tensor shapes, dtypes, devices and contiguity, turns torch tensors into
+raw device pointers and calls the C entry point of the same name on the current CUDA stream.  All
+arithmetic runs in the library's CUDA kernels; there is no CPU or PyTorch fallback — if the shared
+library is missing or fails to load, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpagedattn.so")
+
+PA_BF16, PA_FP16, PA_FP32 = 0, 1, 2
+_DTYPE_CODES = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16, torch.float32: PA_FP32}
+
+PA_OK, PA_EINVAL, PA_EDTYPE, PA_ERANGE, PA_EWORKSPACE, PA_ECUDA, PA_EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+PA_OPT_CHECKED, PA_OPT_DECODE_KERNEL, PA_OPT_PARTITION_TOKENS, PA_OPT_PREFILL_KERNEL = 1, 2, 3, 4
+PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT, PA_DEVERR_CONTEXT_LEN = 1, 2, 4
+PA_DEVERR_COPY_PAIR, PA_DEVERR_QUERY_LOC, PA_DEVERR_TIMEOUT = 8, 16, 32
+
+_vp, _i64, _i32, _sz, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+
+# name -> (restype, argtypes), mirroring include/pagedattn.h
+SIGNATURES = {
+    "paged_kv_write": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp]),
+    "paged_attention_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _i64, _i32, _f32, _i32, _i32,
+                                      _i32, _i32, _vp, _sz, _vp]),
+    "paged_attention_decode_workspace_size": (_sz, [_i32, _i64, _i32, _i32, _i32, _i32]),
+    "paged_attention_prefill": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i32, _i64, _i32, _f32,
+                                       _i32, _i32, _i32, _i32, _vp]),
+    "copy_blocks": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "paged_attention_lse_merge": (_i32, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp]),
+    "pa_set_option": (_i32, [_i32, _i64]),
+    "pa_get_option": (_i64, [_i32]),
+    "pa_last_cuda_error": (_i32, []),
+    "pa_status_string": (ctypes.c_char_p, [_i32]),
+    "pa_device_error_flags": (_i32, [_i32, _vp]),
+    "pa_launch_count": (ctypes.c_uint64, []),
+    "pa_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        super().__init__(f"{fn} failed with status {status} ({detail})")
+
+
+def load_library(path: str | None = None):
+    """Load libpagedattn.so (built in-tree by build.py) and bind its signatures.  Raises if missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or os.environ.get("PAGEDATTN_LIB", LIB_PATH)
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with `python -m pagedattention_kv_cache_paged_gb300.build` "
+                               "(the library has no CPU fallback)")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != PA_OK:
+        lib = load_library()
+        detail = lib.pa_status_string(status).decode()
+        if status == PA_ECUDA:
+            detail += f", cudaError {lib.pa_last_cuda_error()}"
+        raise PagedAttnError(fn, status, detail)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, contiguous: bool = True) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _code(dtype: torch.dtype) -> int:
+    if dtype not in _DTYPE_CODES:
+        raise TypeError(f"unsupported dtype {dtype}")
+    return _DTYPE_CODES[dtype]
+
+
+def _pool_dims(k_pool: torch.Tensor, v_pool: torch.Tensor):
+    if k_pool.dim() != 4 or k_pool.shape != v_pool.shape or k_pool.dtype != v_pool.dtype:
+        raise ValueError("k_pool and v_pool must both be [num_blocks, block_size, n_kv_heads, head_dim] of one dtype")
+    return tuple(int(x) for x in k_pool.shape)
+
+
+# ----------------------------------------------------------------------------------------------
+# entry points
+# ----------------------------------------------------------------------------------------------
+
+def paged_kv_write(k_new, v_new, slot_mapping, k_pool, v_pool, stream=None):
+    """Scatter ``k_new, v_new [T, Hkv, D]`` into the pools at ``slot_mapping`` (int64 [T])."""
+    lib = load_library()
+    NB, S, Hkv, D = _pool_dims(k_pool, v_pool)
+    T = int(slot_mapping.numel())
+    if k_new.shape != (T, Hkv, D) or v_new.shape != (T, Hkv, D):
+        raise ValueError("k_new / v_new must be [T, n_kv_heads, head_dim] matching slot_mapping")
+    dt = k_pool.dtype
+    st = lib.paged_kv_write(_dev(k_new, "k_new", dt), _dev(v_new, "v_new", dt),
+                            _dev(slot_mapping, "slot_mapping", torch.int64), T, _dev(k_pool, "k_pool", dt),
+                            _dev(v_pool, "v_pool", dt), NB, S, Hkv, D, _code(dt), _stream(stream))
+    _check("paged_kv_write", st)
+
+
+_ws_cache: dict = {}
+
+
+def decode_workspace_size(batch: int, block_table_stride: int, block_size: int, n_q_heads: int,
+                          n_kv_heads: int, head_dim: int) -> int:
+    lib = load_library()
+    return int(lib.paged_attention_decode_workspace_size(batch, block_table_stride, block_size, n_q_heads,
+                                                         n_kv_heads, head_dim))
+
+
+def _workspace(device: torch.device, nbytes: int) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    key = (device.index if device.index is not None else torch.cuda.current_device())
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def paged_attention_decode(q, k_pool, v_pool, block_table, context_lens, scale=None, out=None,
+                           workspace="auto", stream=None):
+    """Decode attention: ``q [B, Hq, D]`` over the paged context of each sequence -> ``out [B, Hq, D]``.
+
+    ``workspace``: "auto" (a cached device buffer of the size the library asks for), None (no
+    split-K), or a caller-owned uint8 CUDA tensor."""
+    lib = load_library()
+    NB, S, Hkv, D = _pool_dims(k_pool, v_pool)
+    if q.dim() != 3 or q.shape[2] != D:
+        raise ValueError("q must be [batch, n_q_heads, head_dim]")
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    if block_table.dim() != 2 or block_table.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_table must be [batch, max_blocks] and context_lens [batch]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dt = k_pool.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    bt_stride = int(block_table.stride(0))
+    if block_table.stride(1) != 1:
+        raise ValueError("block_table rows must be contiguous")
+    if workspace == "auto":
+        ws = _workspace(q.device, decode_workspace_size(B, bt_stride, S, Hq, Hkv, D))
+    else:
+        ws = workspace
+    ws_ptr = _dev(ws, "workspace", torch.uint8) if ws is not None else None
+    ws_bytes = int(ws.numel()) if ws is not None else 0
+    st = lib.paged_attention_decode(_dev(out, "out", dt), _dev(q, "q", dt), _dev(k_pool, "k_pool", dt),
+                                    _dev(v_pool, "v_pool", dt),
+                                    _dev(block_table, "block_table", torch.int32, contiguous=False), bt_stride,
+                                    _dev(context_lens, "context_lens", torch.int32), B, NB, S, float(scale),
+                                    Hq, Hkv, D, _code(dt), ws_ptr, ws_bytes, _stream(stream))
+    _check("paged_attention_decode", st)
+    return out
+
+
+def paged_attention_prefill(q, query_start_loc, k_pool, v_pool, block_table, context_lens, scale=None,
+                            out=None, stream=None):
+    """Causal chunked prefill: ``q [total_q, Hq, D]`` (chunks delimited by ``query_start_loc``) over
+    each sequence's paged context -> ``out [total_q, Hq, D]``."""
+    lib = load_library()
+    NB, S, Hkv, D = _pool_dims(k_pool, v_pool)
+    if q.dim() != 3 or q.shape[2] != D:
+        raise ValueError("q must be [total_q, n_q_heads, head_dim]")
+    total_q, Hq = int(q.shape[0]), int(q.shape[1])
+    B = int(context_lens.numel())
+    if query_start_loc.numel() != B + 1 or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("query_start_loc must be [batch + 1] and block_table [batch, max_blocks]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dt = k_pool.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    if block_table.stride(1) != 1:
+        raise ValueError("block_table rows must be contiguous")
+    st = lib.paged_attention_prefill(_dev(out, "out", dt), _dev(q, "q", dt),
+                                     _dev(query_start_loc, "query_start_loc", torch.int32), total_q,
+                                     _dev(k_pool, "k_pool", dt), _dev(v_pool, "v_pool", dt),
+                                     _dev(block_table, "block_table", torch.int32, contiguous=False),
+                                     int(block_table.stride(0)), _dev(context_lens, "context_lens", torch.int32),
+                                     B, NB, S, float(scale), Hq, Hkv, D, _code(dt), _stream(stream))
+    _check("paged_attention_prefill", st)
+    return out
+
+
+def copy_blocks(k_pool, v_pool, block_pairs, stream=None):
+    """Copy-on-write block copies: for each ``(src, dst)`` row of int64 ``block_pairs [n, 2]``."""
+    lib = load_library()
+    NB, S, Hkv, D = _pool_dims(k_pool, v_pool)
+    n = int(block_pairs.shape[0]) if block_pairs.numel() else 0
+    if block_pairs.numel() and (block_pairs.dim() != 2 or block_pairs.shape[1] != 2):
+        raise ValueError("block_pairs must be [n, 2]")
+    block_bytes = S * Hkv * D * k_pool.element_size()
+    st = lib.copy_blocks(_dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+                         _dev(block_pairs, "block_pairs", torch.int64) if n else None, n, NB, block_bytes,
+                         _stream(stream))
+    _check("copy_blocks", st)
+
+
+def paged_attention_lse_merge(part_max, part_sum, part_acc, out_dtype=torch.bfloat16, out=None, stream=None):
+    """Merge split-K partials ``part_max, part_sum [rows, P]`` and ``part_acc [rows, P, D]`` (fp32,
+    log2 domain) -> ``out [rows, D]``."""
+    lib = load_library()
+    rows, P, D = (int(x) for x in part_acc.shape)
+    if out is None:
+        out = torch.empty((rows, D), dtype=out_dtype, device=part_acc.device)
+    st = lib.paged_attention_lse_merge(_dev(out, "out", out.dtype), _dev(part_max, "part_max", torch.float32),
+                                       _dev(part_sum, "part_sum", torch.float32),
+                                       _dev(part_acc, "part_acc", torch.float32), rows, P, D, _code(out.dtype),
+                                       _stream(stream))
+    _check("paged_attention_lse_merge", st)
+    return out
+
+
+def set_option(option: int, value: int):
+    _check("pa_set_option", load_library().pa_set_option(option, int(value)))
+
+
+def get_option(option: int) -> int:
+    return int(load_library().pa_get_option(option))
+
+
+def device_error_flags(clear: bool = True, stream=None) -> int:
+    v = load_library().pa_device_error_flags(1 if clear else 0, _stream(stream))
+    if v < 0:
+        _check("pa_device_error_flags", v)
+    return v
+
+
+def launch_count() -> int:
+    return int(load_library().pa_launch_count())
+
+
+def version() -> str:
+    return load_library().pa_version().decode()

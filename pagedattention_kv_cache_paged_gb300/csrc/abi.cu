@@ -1,0 +1,438 @@
+// The C ABI (include/pagedattn.h): argument validation, the optional checked mode, split-K
+// planning and dispatch to the kernels.  Holds no arithmetic of the method itself.
+#include <atomic>
+#include <cstdio>
+#include <mutex>
+#include <unordered_set>
+#include <vector>
+
+#include "pa_internal.h"
+
+// Device error word, one per device context.  Kernels receive its address as an argument.
+__device__ unsigned int g_pa_device_error = 0;
+
+namespace pa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int64_t> g_options[8] = {};
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_dev_mutex;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+thread_local int t_last_cuda_error = 0;
+
+int fail_cuda(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return PA_ECUDA;
+}
+
+// Address of this device's error word and its SM count, looked up once per device.
+int device_info(unsigned** err, int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return PA_EINVAL;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_pa_device_error);
+    if (e != cudaSuccess) return fail_cuda(e);
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+    g_sm_count[dev] = n;
+  }
+  if (err) *err = g_err_ptr[dev];
+  if (sms) *sms = g_sm_count[dev];
+  return PA_OK;
+}
+
+int finish(cudaError_t e, int launches) {
+  g_launches.fetch_add((uint64_t)launches, std::memory_order_relaxed);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return PA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+int log2i(int64_t x) {
+  int r = 0;
+  while ((int64_t(1) << r) < x) ++r;
+  return r;
+}
+bool checked() { return g_options[PA_OPT_CHECKED].load() != 0; }
+
+int check_dtype(pa_dtype dt) { return (dt == PA_BF16 || dt == PA_FP16 || dt == PA_FP32) ? PA_OK : PA_EDTYPE; }
+
+int check_heads(int n_q_heads, int n_kv_heads, int head_dim) {
+  if (n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return PA_EINVAL;
+  if (n_q_heads % n_kv_heads != 0) return PA_EINVAL;
+  const int g = n_q_heads / n_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return PA_EUNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_EUNSUPPORTED;
+  return PA_OK;
+}
+
+template <typename T>
+int copy_to_host(std::vector<T>& dst, const T* src, int64_t n, cudaStream_t s) {
+  dst.resize((size_t)n);
+  if (n == 0) return PA_OK;
+  cudaError_t e = cudaMemcpyAsync(dst.data(), src, sizeof(T) * (size_t)n, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? PA_OK : fail_cuda(e);
+}
+
+// Checked mode: every table entry a context reaches must name a pool block.
+int validate_tables(const int32_t* block_table, int64_t bt_stride, const int32_t* context_lens, int batch,
+                    int64_t num_blocks, int block_size, cudaStream_t s, std::vector<int32_t>* lens_out) {
+  std::vector<int32_t> lens, table;
+  int rc = copy_to_host(lens, context_lens, batch, s);
+  if (rc) return rc;
+  rc = copy_to_host(table, block_table, (int64_t)batch * bt_stride, s);
+  if (rc) return rc;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t n = lens[b];
+    if (n < 0 || n > bt_stride * block_size) return PA_ERANGE;
+    const int64_t nb = (n + block_size - 1) / block_size;
+    for (int64_t j = 0; j < nb; ++j) {
+      const int64_t id = table[(size_t)(b * bt_stride + j)];
+      if (id < 0 || id >= num_blocks) return PA_ERANGE;
+    }
+  }
+  if (lens_out) *lens_out = std::move(lens);
+  return PA_OK;
+}
+
+// Split-K plan: partition length in tokens and partitions per row.
+void plan_split(int64_t bt_stride, int block_size, int* part_tokens, int* max_parts) {
+  const int64_t max_len = bt_stride * block_size;
+  int64_t p = g_options[PA_OPT_PARTITION_TOKENS].load();
+  if (p <= 0) p = 512;
+  p = ((p + block_size - 1) / block_size) * block_size;
+  if (p >= max_len) {
+    *part_tokens = (int)(max_len > 0 ? max_len : block_size);
+    *max_parts = 1;
+    return;
+  }
+  *part_tokens = (int)p;
+  *max_parts = (int)((max_len + p - 1) / p);
+}
+
+struct WsLayout {
+  size_t bytes;
+  size_t off_m, off_l;
+};
+
+WsLayout workspace_layout(int64_t rows_heads, int max_parts, int head_dim) {
+  WsLayout w{};
+  if (max_parts <= 1) return w;
+  const size_t n = (size_t)rows_heads * (size_t)max_parts;
+  w.off_m = n * (size_t)head_dim * sizeof(float);
+  w.off_l = w.off_m + ((n * sizeof(float) + 15) & ~size_t(15));
+  w.bytes = w.off_l + ((n * sizeof(float) + 15) & ~size_t(15));
+  return w;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_set_option(int option, int64_t value) {
+  switch (option) {
+    case PA_OPT_CHECKED:
+      if (value != 0 && value != 1) return PA_EINVAL;
+      break;
+    case PA_OPT_DECODE_KERNEL:
+    case PA_OPT_PREFILL_KERNEL:
+      if (value < 0 || value > 2) return PA_EINVAL;
+      break;
+    case PA_OPT_PARTITION_TOKENS:
+      if (value < 0 || value > (int64_t(1) << 30)) return PA_EINVAL;
+      break;
+    default:
+      return PA_EINVAL;
+  }
+  g_options[option].store(value);
+  return PA_OK;
+}
+
+int64_t pa_get_option(int option) {
+  if (option < 1 || option > 4) return PA_EINVAL;
+  return g_options[option].load();
+}
+
+int pa_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_EINVAL: return "invalid argument";
+    case PA_EDTYPE: return "unsupported dtype";
+    case PA_ERANGE: return "index, length or pair out of range (checked mode)";
+    case PA_EWORKSPACE: return "workspace too small or misaligned";
+    case PA_ECUDA: return "CUDA launch failed";
+    case PA_EUNSUPPORTED: return "unsupported shape";
+    default: return "unknown status";
+  }
+}
+
+uint64_t pa_launch_count(void) { return g_launches.load(); }
+
+const char* pa_version(void) { return "pagedattn 0.1 (sm_103a)"; }
+
+int pa_device_error_flags(int clear, void* stream) {
+  unsigned* err = nullptr;
+  int rc = device_info(&err, nullptr);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, err, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(err, 0, sizeof(unsigned), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return (int)v;
+}
+
+int paged_kv_write(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens,
+                   void* k_pool, void* v_pool, int64_t num_blocks, int block_size, int n_kv_heads,
+                   int head_dim, pa_dtype dtype, void* stream) {
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  if (n_tokens < 0 || num_blocks <= 0 || block_size <= 0 || n_kv_heads <= 0 || head_dim <= 0) return PA_EINVAL;
+  if (n_tokens == 0) return PA_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool) return PA_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool)) return PA_EINVAL;
+  const int64_t row_bytes = (int64_t)n_kv_heads * head_dim * dtype_bytes(dtype);
+  if (row_bytes % 16 != 0) return PA_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned* err = nullptr;
+  rc = device_info(&err, nullptr);
+  if (rc) return rc;
+  const int64_t total_slots = num_blocks * block_size;
+  if (checked()) {
+    std::vector<int64_t> slots;
+    rc = copy_to_host(slots, slot_mapping, n_tokens, s);
+    if (rc) return rc;
+    std::unordered_set<int64_t> seen;
+    for (int64_t v : slots) {
+      if (v < 0) continue;
+      if (v >= total_slots || !seen.insert(v).second) return PA_ERANGE;
+    }
+  }
+  KvWriteArgs a{k_new, v_new, slot_mapping, n_tokens, k_pool, v_pool, total_slots, (int)(row_bytes / 16), err};
+  int launches = 0;
+  cudaError_t e = launch_kv_write(a, dtype, s, &launches);
+  return finish(e, launches);
+}
+
+size_t paged_attention_decode_workspace_size(int batch, int64_t block_table_stride, int block_size,
+                                             int n_q_heads, int n_kv_heads, int head_dim) {
+  (void)n_kv_heads;
+  if (batch <= 0 || block_table_stride <= 0 || block_size <= 0 || n_q_heads <= 0 || head_dim <= 0) return 0;
+  int part = 0, max_parts = 1;
+  plan_split(block_table_stride, block_size, &part, &max_parts);
+  return workspace_layout((int64_t)batch * n_q_heads, max_parts, head_dim).bytes;
+}
+
+int paged_attention_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_table, int64_t block_table_stride,
+                           const int32_t* context_lens, int batch, int64_t num_blocks, int block_size,
+                           float scale, int n_q_heads, int n_kv_heads, int head_dim, pa_dtype dtype,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  rc = check_heads(n_q_heads, n_kv_heads, head_dim);
+  if (rc) return rc;
+  if (batch < 0 || num_blocks <= 0 || block_table_stride <= 0 || !is_pow2(block_size) || block_size > 256)
+    return block_size > 256 || (block_size > 0 && !is_pow2(block_size)) ? PA_EUNSUPPORTED : PA_EINVAL;
+  if (batch == 0) return PA_OK;
+  if (!out || !q || !k_pool || !v_pool || !block_table || !context_lens) return PA_EINVAL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PA_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned* err = nullptr;
+  int sms = 0;
+  rc = device_info(&err, &sms);
+  if (rc) return rc;
+  if (checked()) {
+    rc = validate_tables(block_table, block_table_stride, context_lens, batch, num_blocks, block_size, s, nullptr);
+    if (rc) return rc;
+  }
+  const int64_t kernel_opt = g_options[PA_OPT_DECODE_KERNEL].load();
+  if (kernel_opt == 2) return PA_EUNSUPPORTED;
+
+  int part_tokens = 0, max_parts = 1;
+  plan_split(block_table_stride, block_size, &part_tokens, &max_parts);
+  WsLayout ws = workspace_layout((int64_t)batch * n_q_heads, max_parts, head_dim);
+  if (max_parts > 1) {
+    if (workspace == nullptr) {
+      max_parts = 1;
+      part_tokens = (int)(block_table_stride * block_size);
+    } else if (workspace_bytes < ws.bytes || !aligned16(workspace)) {
+      return PA_EWORKSPACE;
+    }
+  }
+  AttnArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.block_table = block_table;
+  a.bt_stride = block_table_stride;
+  a.context_lens = context_lens;
+  a.query_start_loc = nullptr;
+  a.batch = batch;
+  a.rows = batch;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.block_shift = log2i(block_size);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.n_q_heads = n_q_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.group = n_q_heads / n_kv_heads;
+  a.head_dim = head_dim;
+  a.part_tokens = part_tokens;
+  a.max_parts = max_parts;
+  if (max_parts > 1) {
+    char* base = static_cast<char*>(workspace);
+    a.ws_acc = reinterpret_cast<float*>(base);
+    a.ws_m = reinterpret_cast<float*>(base + ws.off_m);
+    a.ws_l = reinterpret_cast<float*>(base + ws.off_l);
+  }
+  a.err = err;
+  int launches = 0;
+  cudaError_t e = launch_attn_simt(a, dtype, s, &launches);
+  if (e == cudaSuccess && max_parts > 1) {
+    MergeArgs m{};
+    m.out = out;
+    m.part_m = a.ws_m;
+    m.part_l = a.ws_l;
+    m.part_acc = a.ws_acc;
+    m.rows = (int64_t)batch * n_q_heads;
+    m.n_parts = max_parts;
+    m.head_dim = head_dim;
+    m.context_lens = context_lens;
+    m.heads_per_seq = n_q_heads;
+    m.part_tokens = part_tokens;
+    m.max_len = block_table_stride * block_size;
+    e = launch_lse_merge(m, dtype, s, &launches);
+  }
+  return finish(e, launches);
+}
+
+int paged_attention_prefill(void* out, const void* q, const int32_t* query_start_loc, int64_t total_q,
+                            const void* k_pool, const void* v_pool, const int32_t* block_table,
+                            int64_t block_table_stride, const int32_t* context_lens, int batch,
+                            int64_t num_blocks, int block_size, float scale, int n_q_heads,
+                            int n_kv_heads, int head_dim, pa_dtype dtype, void* stream) {
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  rc = check_heads(n_q_heads, n_kv_heads, head_dim);
+  if (rc) return rc;
+  if (batch < 0 || total_q < 0 || num_blocks <= 0 || block_table_stride <= 0) return PA_EINVAL;
+  if (!is_pow2(block_size) || block_size > 256) return block_size <= 0 ? PA_EINVAL : PA_EUNSUPPORTED;
+  if (batch == 0 || total_q == 0) return PA_OK;
+  if (!out || !q || !query_start_loc || !k_pool || !v_pool || !block_table || !context_lens) return PA_EINVAL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PA_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned* err = nullptr;
+  rc = device_info(&err, nullptr);
+  if (rc) return rc;
+  if (checked()) {
+    std::vector<int32_t> lens, qsl;
+    rc = validate_tables(block_table, block_table_stride, context_lens, batch, num_blocks, block_size, s, &lens);
+    if (rc) return rc;
+    rc = copy_to_host(qsl, query_start_loc, (int64_t)batch + 1, s);
+    if (rc) return rc;
+    if (qsl[0] != 0 || qsl[(size_t)batch] != total_q) return PA_ERANGE;
+    for (int b = 0; b < batch; ++b) {
+      const int64_t m = (int64_t)qsl[(size_t)b + 1] - qsl[(size_t)b];
+      if (m < 0 || m > lens[(size_t)b]) return PA_ERANGE;
+    }
+  }
+  if (g_options[PA_OPT_PREFILL_KERNEL].load() == 2) return PA_EUNSUPPORTED;
+  AttnArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.block_table = block_table;
+  a.bt_stride = block_table_stride;
+  a.context_lens = context_lens;
+  a.query_start_loc = query_start_loc;
+  a.batch = batch;
+  a.rows = total_q;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.block_shift = log2i(block_size);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.n_q_heads = n_q_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.group = n_q_heads / n_kv_heads;
+  a.head_dim = head_dim;
+  a.part_tokens = (int)(block_table_stride * block_size);
+  a.max_parts = 1;
+  a.err = err;
+  int launches = 0;
+  cudaError_t e = launch_attn_simt(a, dtype, s, &launches);
+  return finish(e, launches);
+}
+
+int copy_blocks(void* k_pool, void* v_pool, const int64_t* block_pairs, int64_t n_pairs,
+                int64_t num_blocks, int64_t block_bytes, void* stream) {
+  if (n_pairs < 0 || num_blocks <= 0 || block_bytes <= 0 || block_bytes % 16 != 0) return PA_EINVAL;
+  if (n_pairs == 0) return PA_OK;
+  if (!k_pool || !v_pool || !block_pairs) return PA_EINVAL;
+  if (!aligned16(k_pool) || !aligned16(v_pool)) return PA_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned* err = nullptr;
+  int rc = device_info(&err, nullptr);
+  if (rc) return rc;
+  if (checked()) {
+    std::vector<int64_t> pairs;
+    rc = copy_to_host(pairs, block_pairs, 2 * n_pairs, s);
+    if (rc) return rc;
+    std::unordered_set<int64_t> dsts, srcs;
+    for (int64_t i = 0; i < n_pairs; ++i) {
+      const int64_t src = pairs[(size_t)(2 * i)], dst = pairs[(size_t)(2 * i + 1)];
+      if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) return PA_ERANGE;
+      if (!dsts.insert(dst).second) return PA_ERANGE;
+      srcs.insert(src);
+    }
+    for (int64_t d : dsts)
+      if (srcs.count(d)) return PA_ERANGE;
+  }
+  CopyBlocksArgs a{k_pool, v_pool, block_pairs, n_pairs, num_blocks, block_bytes / 16, err};
+  int launches = 0;
+  cudaError_t e = launch_copy_blocks(a, s, &launches);
+  return finish(e, launches);
+}
+
+int paged_attention_lse_merge(void* out, const float* part_max, const float* part_sum,
+                              const float* part_acc, int64_t rows, int n_parts, int head_dim,
+                              pa_dtype dtype, void* stream) {
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  if (rows < 0 || n_parts <= 0) return PA_EINVAL;
+  if (head_dim != 64 && head_dim != 128) return PA_EUNSUPPORTED;
+  if (rows == 0) return PA_OK;
+  if (!out || !part_max || !part_sum || !part_acc) return PA_EINVAL;
+  MergeArgs m{};
+  m.out = out;
+  m.part_m = part_max;
+  m.part_l = part_sum;
+  m.part_acc = part_acc;
+  m.rows = rows;
+  m.n_parts = n_parts;
+  m.head_dim = head_dim;
+  m.context_lens = nullptr;
+  int launches = 0;
+  cudaError_t e = launch_lse_merge(m, dtype, static_cast<cudaStream_t>(stream), &launches);
+  return finish(e, launches);
+}
+
+}  // extern "C"

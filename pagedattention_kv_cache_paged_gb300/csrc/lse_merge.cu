@@ -1,0 +1,85 @@
+// Log-sum-exp merge of split-K partials.
+//
+// Partition p of a row holds m_p (maximum score, log2 domain), l_p = sum 2^(s - m_p) and the
+// unnormalised accumulator acc_p = sum 2^(s - m_p) v.  Rescaling every partition to the common
+// maximum M = max_p m_p gives the exact softmax over the union:
+//   out = sum_p acc_p 2^(m_p - M) / sum_p l_p 2^(m_p - M).
+// This is the correction step of the single-pass softmax (JuliaPagedAttn README, "Online
+// Softmax") applied to whole partitions instead of single tokens.  Partitions with l_p = 0 hold no
+// token and are skipped; a row with none left is written as zeros.
+//
+// One warp per output row; lanes own head_dim / 32 consecutive elements.
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+constexpr int kMergeWarps = 4;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const MergeArgs a) {
+  constexpr int kPer = D / 32;
+  const int64_t row = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= a.rows) return;
+  int parts = a.n_parts;
+  if (a.context_lens != nullptr) {
+    int64_t len = __ldg(a.context_lens + row / a.heads_per_seq);
+    len = len < 0 ? 0 : (len > a.max_len ? a.max_len : len);
+    parts = len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
+    if (parts <= 1) return;  // written directly by the partition kernel
+  }
+  const float* pm = a.part_m + row * a.n_parts;
+  const float* pl = a.part_l + row * a.n_parts;
+  float M = -INFINITY;
+  for (int p = lane; p < parts; p += 32)
+    if (pl[p] > 0.f) M = fmaxf(M, pm[p]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float L = 0.f;
+  float acc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  if (M != -INFINITY) {
+    const float* pa_ = a.part_acc + row * a.n_parts * (int64_t)D + lane * kPer;
+    for (int p = 0; p < parts; ++p) {
+      const float lp = pl[p];
+      if (!(lp > 0.f)) continue;
+      const float f = fast_exp2(pm[p] - M);
+      L = fmaf(lp, f, L);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) acc[i] = fmaf(pa_[(int64_t)p * D + i], f, acc[i]);
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  T* o = static_cast<T*>(a.out) + row * D + lane * kPer;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) o[i] = Elt<T>::from_float(acc[i] * inv);
+}
+
+template <typename T>
+static cudaError_t launch_merge_t(const MergeArgs& a, cudaStream_t s) {
+  const int64_t blocks = (a.rows + kMergeWarps - 1) / kMergeWarps;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  switch (a.head_dim) {
+    case 64: lse_merge_kernel<T, 64><<<(unsigned)blocks, kMergeWarps * 32, 0, s>>>(a); break;
+    case 128: lse_merge_kernel<T, 128><<<(unsigned)blocks, kMergeWarps * 32, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(const MergeArgs& a, pa_dtype dt, cudaStream_t s, int* launches) {
+  if (a.rows == 0) return cudaSuccess;
+  cudaError_t e;
+  switch (dt) {
+    case PA_BF16: e = launch_merge_t<__nv_bfloat16>(a, s); break;
+    case PA_FP16: e = launch_merge_t<__half>(a, s); break;
+    case PA_FP32: e = launch_merge_t<float>(a, s); break;
+    default: return cudaErrorInvalidValue;
+  }
+  ++*launches;
+  return e;
+}
+
+}  // namespace pa

@@ -1,0 +1,89 @@
+// Internal launch interface between the C ABI layer (abi.cu) and the kernel translation units.
+// Host-only declarations; no torch types, no device code.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedattn.h"
+
+namespace pa {
+
+// Element size of an I/O dtype in bytes.
+inline int dtype_bytes(pa_dtype dt) { return dt == PA_FP32 ? 4 : 2; }
+
+struct KvWriteArgs {
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+  int64_t n_tokens;
+  void* k_pool;
+  void* v_pool;
+  int64_t total_slots;   // num_blocks * block_size
+  int row_vecs;          // n_kv_heads * head_dim * elt / 16 (16-byte vectors per token row)
+  unsigned* err;         // device error word
+};
+
+struct CopyBlocksArgs {
+  void* k_pool;
+  void* v_pool;
+  const int64_t* pairs;
+  int64_t n_pairs;
+  int64_t num_blocks;
+  int64_t block_vecs;    // block_bytes / 16
+  unsigned* err;
+};
+
+// One attention launch over "rows": a decode row is a sequence, a prefill row is a query token.
+struct AttnArgs {
+  void* out;
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* context_lens;
+  const int32_t* query_start_loc;  // nullptr for decode
+  int batch;
+  int64_t rows;                    // batch (decode) or total_q (prefill)
+  int64_t num_blocks;
+  int block_size;
+  int block_shift;                 // log2(block_size)
+  float scale_log2;                // scale * log2(e)
+  int n_q_heads;
+  int n_kv_heads;
+  int group;                       // n_q_heads / n_kv_heads
+  int head_dim;
+  // split-K (decode only)
+  int part_tokens;                 // tokens per partition (multiple of block_size)
+  int max_parts;                   // partitions per row in the grid (1 = no split)
+  float* ws_m;                     // [rows * n_q_heads][max_parts]
+  float* ws_l;                     // [rows * n_q_heads][max_parts]
+  float* ws_acc;                   // [rows * n_q_heads][max_parts][head_dim]
+  unsigned* err;
+};
+
+struct MergeArgs {
+  void* out;
+  const float* part_m;
+  const float* part_l;
+  const float* part_acc;
+  int64_t rows;                    // rows of [rows][n_parts]
+  int n_parts;
+  int head_dim;
+  // when context_lens != nullptr, row r belongs to sequence r / heads_per_seq and only its first
+  // ceil(len / part_tokens) partitions exist; rows with a single partition are skipped (the
+  // partition kernel wrote them directly).
+  const int32_t* context_lens;
+  int heads_per_seq;
+  int part_tokens;
+  int64_t max_len;                 // clamp for context_lens (bt_stride * block_size)
+};
+
+// Launchers: return cudaSuccess or the launch error.  `launches` is incremented per kernel.
+cudaError_t launch_kv_write(const KvWriteArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
+cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t s, int* launches);
+cudaError_t launch_attn_simt(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
+cudaError_t launch_lse_merge(const MergeArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
+
+}  // namespace pa

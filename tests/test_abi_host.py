@@ -1,0 +1,108 @@
+"""Host-only checks of the C ABI: the library builds/loads, exports every function include/*.h
+declares, and rejects bad arguments before touching a GPU.  No compute call is made here."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import pagedattention_kv_cache_paged_gb300 as pa
+from pagedattention_kv_cache_paged_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^PA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_abi.LIB_PATH):
+        from pagedattention_kv_cache_paged_gb300 import build
+        build.build()
+    return pa.load_library()
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    names = _declared_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _abi.SIGNATURES, n
+    assert set(_abi.SIGNATURES) == set(names)
+
+
+def test_version_and_status_strings(lib):
+    assert b"sm_103a" in lib.pa_version()
+    assert lib.pa_status_string(pa.PA_ERANGE) != lib.pa_status_string(0)
+
+
+def test_options_validate(lib):
+    assert lib.pa_set_option(999, 1) == pa.PA_EINVAL
+    assert lib.pa_set_option(pa.PA_OPT_CHECKED, 2) == pa.PA_EINVAL
+    assert lib.pa_set_option(pa.PA_OPT_DECODE_KERNEL, 3) == pa.PA_EINVAL
+    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 256) == 0
+    assert lib.pa_get_option(pa.PA_OPT_PARTITION_TOKENS) == 256
+    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 0) == 0
+
+
+def test_argument_errors_are_returned_before_any_launch(lib):
+    n = None
+    # bad dtype
+    assert lib.paged_kv_write(n, n, n, 1, n, n, 4, 16, 2, 64, 7, n) == pa.PA_EDTYPE
+    # zero tokens is a no-op
+    assert lib.paged_kv_write(n, n, n, 0, n, n, 4, 16, 2, 64, pa.PA_BF16, n) == 0
+    # null pointers
+    assert lib.paged_kv_write(n, n, n, 3, n, n, 4, 16, 2, 64, pa.PA_BF16, n) == pa.PA_EINVAL
+    # heads not divisible / unsupported group / unsupported head_dim / bad block size
+    args = [n, n, n, n, n, 4, n, 2, 8, 16, 1.0]
+    assert lib.paged_attention_decode(*args, 6, 4, 64, pa.PA_BF16, n, 0, n) == pa.PA_EINVAL
+    assert lib.paged_attention_decode(*args, 48, 3, 64, pa.PA_BF16, n, 0, n) == pa.PA_EUNSUPPORTED
+    assert lib.paged_attention_decode(*args, 8, 2, 96, pa.PA_BF16, n, 0, n) == pa.PA_EUNSUPPORTED
+    bad_bs = [n, n, n, n, n, 4, n, 2, 8, 12, 1.0]
+    assert lib.paged_attention_decode(*bad_bs, 8, 2, 64, pa.PA_BF16, n, 0, n) == pa.PA_EUNSUPPORTED
+    # batch 0 is a no-op
+    zero = [n, n, n, n, n, 4, n, 0, 8, 16, 1.0]
+    assert lib.paged_attention_decode(*zero, 8, 2, 64, pa.PA_BF16, n, 0, n) == 0
+    # copy_blocks: block bytes must be a multiple of 16
+    assert lib.copy_blocks(n, n, n, 1, 4, 24, n) == pa.PA_EINVAL
+    assert lib.copy_blocks(n, n, n, 0, 4, 32, n) == 0
+    # merge
+    assert lib.paged_attention_lse_merge(n, n, n, n, 4, 0, 64, pa.PA_BF16, n) == pa.PA_EINVAL
+    assert lib.paged_attention_lse_merge(n, n, n, n, 4, 2, 80, pa.PA_BF16, n) == pa.PA_EUNSUPPORTED
+
+
+def test_workspace_size_follows_the_partition_plan(lib):
+    f = lib.paged_attention_decode_workspace_size
+    # short tables never split
+    assert f(64, 8, 16, 32, 8, 128) == 0
+    # 4096-token tables at the default 512-token partitions: 8 partitions of (128 + 2) floats
+    ws = f(64, 256, 16, 32, 8, 128)
+    assert ws >= 64 * 32 * 8 * 130 * 4
+    assert ws % 16 == 0
+    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 1024) == 0
+    assert f(64, 256, 16, 32, 8, 128) < ws
+    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 0) == 0
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    kp = torch.zeros((4, 16, 2, 64))
+    with pytest.raises(ValueError):
+        pa.paged_kv_write(torch.zeros((1, 2, 64)), torch.zeros((1, 2, 64)), torch.zeros(1, dtype=torch.int64),
+                          kp, kp.clone())
+
+
+def test_library_source_has_no_oracle_dependency():
+    pkg = os.path.join(ROOT, "pagedattention_kv_cache_paged_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):
+        if path.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+            text = open(path).read()
+            assert "oracle" not in text.replace("no oracle", ""), path
