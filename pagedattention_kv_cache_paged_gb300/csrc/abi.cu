@@ -263,7 +263,9 @@ int paged_attention_decode(void* out, const void* q, const void* k_pool, const v
     if (rc) return rc;
   }
   const int64_t kernel_opt = g_options[PA_OPT_DECODE_KERNEL].load();
-  if (kernel_opt == 2) return PA_EUNSUPPORTED;
+  const bool tc_ok = decode_tc_supported(dtype, block_size, head_dim, n_q_heads / n_kv_heads, num_blocks);
+  if (kernel_opt == 2 && !tc_ok) return PA_EUNSUPPORTED;
+  const bool use_tc = kernel_opt == 2 || (kernel_opt == 0 && tc_ok);
 
   int part_tokens = 0, max_parts = 1;
   plan_split(block_table_stride, block_size, &part_tokens, &max_parts);
@@ -305,7 +307,7 @@ int paged_attention_decode(void* out, const void* q, const void* k_pool, const v
   }
   a.err = err;
   int launches = 0;
-  cudaError_t e = launch_attn_simt(a, dtype, s, &launches);
+  cudaError_t e = use_tc ? launch_decode_tc(a, dtype, s, &launches) : launch_attn_simt(a, dtype, s, &launches);
   if (e == cudaSuccess && max_parts > 1) {
     MergeArgs m{};
     m.out = out;

@@ -202,12 +202,12 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(const AttnAr
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kSimtWarps; ++w)
-      if (sm_l[w][h] > 0.f) M = fmaxf(M, sm_m[w][h]);
+      if (sm_l[w][h] != 0.f) M = fmaxf(M, sm_m[w][h]);
     float L = 0.f, A = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kSimtWarps; ++w) {
-        if (sm_l[w][h] > 0.f) {
+        if (sm_l[w][h] != 0.f) {
           const float f = fast_exp2(sm_m[w][h] - M);
           L = fmaf(sm_l[w][h], f, L);
           A = fmaf(sm_acc[w][h][d], f, A);
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(const AttnAr
     const int64_t qh = row * a.n_q_heads + (int64_t)kvh * G + h;  // global (row, query head)
     if (direct) {
       T* o = static_cast<T*>(a.out) + qh * D + d;
-      *o = Elt<T>::from_float(L > 0.f ? A / L : 0.f);
+      *o = Elt<T>::from_float(L != 0.f ? A / L : 0.f);
     } else {
       const int64_t pi = qh * a.max_parts + part;
       a.ws_acc[pi * D + d] = A;

@@ -1,0 +1,385 @@
+// Tensor-core paged decode for bf16/fp16 pools (block_size a multiple of 16).
+//
+// Same contract and grid as the CUDA-core kernel (attn_simt.cu): one CTA per (sequence, KV head,
+// split-K partition) serving the whole GQA query group, online softmax (JuliaPagedAttn README,
+// "Online Softmax"), read-time GQA (nanoserve Day 19, "What I learned" 4), output or partial state
+// for the log-sum-exp merge.  What differs is how the bytes move and how the dots are formed:
+//
+// * Data movement.  A 16-token tile of one KV head (K and V, 2 x 16 x head_dim elements) is
+//   fetched by TMA from the block the table names: the pool is seen as a 2-D tensor
+//   [num_blocks * block_size rows][n_kv_heads * head_dim columns] and each tile is head_dim/64
+//   boxes of 16 rows x 64 columns per operand, written to shared memory with the 128-byte swizzle.
+//   Each warp owns a private ring of kStages tiles guarded by one mbarrier per stage; lane 0
+//   refills a stage as soon as the warp has consumed it, so every warp keeps kStages tiles in
+//   flight with no cross-warp synchronisation (the software prefetch / double buffering of
+//   JuliaPagedAttn's kernel, done by the copy engine).
+// * Arithmetic.  Q K^T and P V are mma.sync m16n8k16 products with fp32 accumulation: the query
+//   group (G <= 8 heads) fills the rows of the A operand, K and V tiles are read with ldmatrix
+//   (V transposed), and the softmax probabilities are re-packed from the QK accumulator registers
+//   straight into the A operand of the PV product.  One online-softmax update per 16-token tile.
+// * Ragged ends.  Tokens past the partition's end are masked to -inf before the softmax and their
+//   V rows are zeroed in shared memory (a stale NaN times a zero probability would otherwise
+//   poison the accumulator).  A tile whose table entry is out of range is skipped and recorded.
+//
+// The tile loop inside a warp visits tokens in increasing logical order, so the result depends
+// only on logical positions, not on where the blocks sit in the pool.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+constexpr int kTcWarps = 4;
+constexpr int kTile = 16;          // tokens per tile (one mma k-step of PV)
+constexpr int kHalfBytes = kTile * 128;  // 16 rows x 64 columns x 2 bytes
+
+template <int D>
+struct TcCfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;  // K and V
+  static constexpr int kStages = D == 128 ? 3 : 6;               // per warp
+  static constexpr int kSmemBytes = 1024 /*barriers*/ + 1024 /*alignment*/ + kTcWarps * kStages * kStageBytes;
+};
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kTcWarps * 32, 2)
+    decode_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap) {
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  constexpr int kHalves = TcCfg<D>::kHalves;
+  constexpr int kStageBytes = TcCfg<D>::kStageBytes;
+  constexpr int kStages = TcCfg<D>::kStages;
+  constexpr int kKSteps = D / 16;
+  constexpr int kDTiles = D / 8;
+  static_assert(G <= 8, "query group must fit the first 8 rows of the mma tile");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base);
+  uint8_t* stages = base + 1024;
+
+  const int kvh = blockIdx.x % a.n_kv_heads;
+  const int64_t rest = blockIdx.x / a.n_kv_heads;
+  const int part = (int)(rest % a.max_parts);
+  const int64_t row = rest / a.max_parts;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane >> 2;   // mma row group: query head g of the group
+  const int tig = lane & 3;  // thread in group
+
+  const int64_t max_len = a.bt_stride << a.block_shift;
+  const int b = (int)row;
+  int64_t len = __ldg(a.context_lens + b);
+  if (len < 0 || len > max_len) {
+    if (threadIdx.x == 0) raise_error(a.err, PA_DEVERR_CONTEXT_LEN);
+    len = len < 0 ? 0 : max_len;
+  }
+  const int n_parts_row = len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
+  if (part >= n_parts_row) return;
+  const int64_t t_begin = (int64_t)part * a.part_tokens;
+  const int64_t t_end = min(t_begin + a.part_tokens, len);
+  const int n_tiles = (int)((t_end - t_begin + kTile - 1) / kTile);
+  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kTcWarps - 1) / kTcWarps : 0;
+
+  const int32_t* table = a.block_table + (int64_t)b * a.bt_stride;
+  const int bmask = a.block_size - 1;
+  uint64_t* my_bars = bars + warp * kStages;
+  uint8_t* my_stages = stages + warp * kStages * kStageBytes;
+
+  // tile j of this warp covers tokens [tile_t0(j), tile_t0(j) + 16)
+  auto tile_t0 = [&](int j) -> int64_t { return t_begin + (int64_t)(warp + kTcWarps * j) * kTile; };
+  auto tile_block = [&](int j) -> int { return __ldg(table + (tile_t0(j) >> a.block_shift)); };
+
+  if (lane == 0) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+    for (int s = 0; s < kStages; ++s) mbar_init(&my_bars[s], 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+
+  auto issue = [&](int j) {  // lane 0 only
+    const int s = j % kStages;
+    const int blk = tile_block(j);
+    if (blk < 0 || blk >= a.num_blocks) {
+      raise_error(a.err, PA_DEVERR_BLOCK_ID);
+      mbar_arrive(&my_bars[s]);  // complete the phase without data; the consumer skips the tile
+      return;
+    }
+    const int y = (int)(((int64_t)blk << a.block_shift) + (tile_t0(j) & bmask));
+    uint8_t* st = my_stages + s * kStageBytes;
+    mbar_arrive_expect_tx(&my_bars[s], kStageBytes);
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h) tma_load_2d(st + h * kHalfBytes, &kmap, kvh * D + h * 64, y, &my_bars[s]);
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h)
+      tma_load_2d(st + (kHalves + h) * kHalfBytes, &vmap, kvh * D + h * 64, y, &my_bars[s]);
+  };
+  if (lane == 0) {
+    const int pre = my_tiles < kStages ? my_tiles : kStages;
+    for (int j = 0; j < pre; ++j) issue(j);
+  }
+
+  // Q fragments of the A operand: rows = query heads, two b32 (4 elements) per k-step per lane.
+  uint32_t qa[kKSteps][2];
+  {
+    const T* qrow = static_cast<const T*>(a.q) + (row * a.n_q_heads + (int64_t)kvh * G + g) * D;
+#pragma unroll
+    for (int ks = 0; ks < kKSteps; ++ks) {
+      if (g < G) {
+        qa[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig));
+        qa[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig));
+      } else {
+        qa[ks][0] = 0u;
+        qa[ks][1] = 0u;
+      }
+    }
+  }
+
+  float o[kDTiles][4];
+#pragma unroll
+  for (int i = 0; i < kDTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;
+  bool timed_out = false;
+
+  for (int j = 0; j < my_tiles; ++j) {
+    const int s = j % kStages;
+    if (!mbar_wait(&my_bars[s], (unsigned)((j / kStages) & 1))) {
+      timed_out = true;
+      break;
+    }
+    const int blk = tile_block(j);
+    const int64_t t0 = tile_t0(j);
+    const int valid = (int)(t_end - t0 < kTile ? t_end - t0 : kTile);
+    uint8_t* st = my_stages + s * kStageBytes;
+    const uint32_t k_base = smem_u32(st);
+    const uint32_t v_base = smem_u32(st + kHalves * kHalfBytes);
+    if (blk >= 0 && blk < a.num_blocks) {
+      if (valid < kTile) {
+        // zero the V rows past the end (both halves): 16-byte stores, rows valid..15
+        const int nz = (kTile - valid) * 8 * kHalves;
+        for (int i = lane; i < nz; i += 32) {
+          const int h = i / ((kTile - valid) * 8);
+          const int r = valid + (i / 8) % (kTile - valid);
+          const int c = i % 8;
+          *reinterpret_cast<uint4*>(st + (kHalves + h) * kHalfBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      // ---- S = Q K^T: two n-tiles of 8 tokens ----------------------------------------------
+      float sc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        const int tok = nt * 8 + (lane & 7);
+#pragma unroll
+        for (int ks = 0; ks < kKSteps; ks += 2) {
+          const int chunk = 2 * ks + (lane >> 3);  // 8-element chunk along head_dim
+          const uint32_t addr = k_base + (chunk >> 3) * kHalfBytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma_16816<kBf16>(sc[nt], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+          mma_16816<kBf16>(sc[nt], qa[ks + 1][0], 0u, qa[ks + 1][1], 0u, b2, b3);
+        }
+      }
+      // ---- online softmax over the tile (rows g, columns = tokens) ---------------------------
+      float x[4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int tok = nt * 8 + 2 * tig + e;
+          x[nt * 2 + e] = tok < valid ? sc[nt][e] * a.scale_log2 : -INFINITY;
+        }
+      }
+      float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+      const float m_new = fmaxf(m_run, tmax);
+      const float corr = fast_exp2(m_run - m_new);
+      float p[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - m_new);
+      l_run = l_run * corr + ((p[0] + p[1]) + (p[2] + p[3]));
+      if (__any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+        for (int i = 0; i < kDTiles; ++i) {
+          o[i][0] *= corr;
+          o[i][1] *= corr;
+        }
+      }
+      m_run = m_new;
+      // ---- O += P V: P from the score registers, V^T fragments by ldmatrix.trans ----------------
+      const uint32_t pa0 = pack2<kBf16>(p[0], p[1]);
+      const uint32_t pa2 = pack2<kBf16>(p[2], p[3]);
+#pragma unroll
+      for (int dt = 0; dt < kDTiles; dt += 2) {
+        const int mi = lane >> 3;
+        const int tok = (lane & 7) + 8 * (mi & 1);
+        const int chunk = dt + (mi >> 1);
+        const uint32_t addr = v_base + (chunk >> 3) * kHalfBytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(addr, b0, b1, b2, b3);
+        mma_16816<kBf16>(o[dt], pa0, 0u, pa2, 0u, b0, b1);
+        mma_16816<kBf16>(o[dt + 1], pa0, 0u, pa2, 0u, b2, b3);
+      }
+    }
+    // release the stage and refill it with this warp's tile j + kStages
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && j + kStages < my_tiles) issue(j + kStages);
+  }
+  if (timed_out && lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+
+  // ---- combine: quad-reduce l, stage (m, l, o) per warp in the warp's own stage 0 --------------
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  __syncwarp();
+  float* wo = reinterpret_cast<float*>(my_stages);  // [G][D] floats, then m[G], l[G]
+  if (g < G) {
+#pragma unroll
+    for (int i = 0; i < kDTiles; ++i) {
+      wo[g * D + i * 8 + 2 * tig] = o[i][0];
+      wo[g * D + i * 8 + 2 * tig + 1] = o[i][1];
+    }
+    if (tig == 0) {
+      wo[G * D + g] = m_run;
+      wo[G * D + G + g] = my_tiles > 0 && !timed_out ? l_run : 0.f;
+    }
+  }
+  __syncthreads();
+
+  const bool direct = n_parts_row == 1;
+  for (int i = threadIdx.x; i < G * D; i += kTcWarps * 32) {
+    const int h = i / D;
+    const int d = i - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kTcWarps; ++w) {
+      const float* ww = reinterpret_cast<const float*>(stages + w * kStages * kStageBytes);
+      if (ww[G * D + G + h] != 0.f) M = fmaxf(M, ww[G * D + h]);
+    }
+    float L = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kTcWarps; ++w) {
+        const float* ww = reinterpret_cast<const float*>(stages + w * kStages * kStageBytes);
+        const float lw = ww[G * D + G + h];
+        if (lw != 0.f) {
+          const float f = fast_exp2(ww[G * D + h] - M);
+          L = fmaf(lw, f, L);
+          A = fmaf(ww[h * D + d], f, A);
+        }
+      }
+    }
+    const int64_t qh = row * a.n_q_heads + (int64_t)kvh * G + h;
+    if (direct) {
+      static_cast<T*>(a.out)[qh * D + d] = Elt<T>::from_float(L != 0.f ? A / L : 0.f);
+    } else {
+      const int64_t pi = qh * a.max_parts + part;
+      a.ws_acc[pi * D + d] = A;
+      if (d == 0) {
+        a.ws_m[pi] = M;
+        a.ws_l[pi] = L;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// host side: tensor maps and dispatch
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+// Pool viewed as [num_blocks * block_size][n_kv_heads * head_dim], boxes of 16 rows x 64 columns.
+bool encode_pool_map(CUtensorMap* map, const void* pool, pa_dtype dt, int64_t num_blocks, int block_size,
+                     int n_kv_heads, int head_dim) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)n_kv_heads * head_dim, (cuuint64_t)num_blocks * block_size};
+  const cuuint64_t strides[1] = {(cuuint64_t)n_kv_heads * head_dim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kTile};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType ty = dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(map, ty, 2, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool decode_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks) {
+  if (dt != PA_BF16 && dt != PA_FP16) return false;
+  if (block_size % kTile != 0) return false;
+  if (head_dim != 64 && head_dim != 128) return false;
+  if (group > 8) return false;
+  if (num_blocks * block_size >= (int64_t(1) << 31)) return false;  // TMA row coordinate is int32
+  return encode_fn() != nullptr;
+}
+
+template <typename T, int D, int G>
+static cudaError_t launch_tc_g(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
+  constexpr int smem = TcCfg<D>::kSmemBytes;
+  static bool attr_set[64] = {};  // per instantiation and device; idempotent, so a race is harmless
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(decode_tc_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const int64_t grid = a.rows * (int64_t)a.max_parts * a.n_kv_heads;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  decode_tc_kernel<T, D, G><<<(unsigned)grid, kTcWarps * 32, smem, s>>>(a, km, vm);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t launch_tc_d(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
+  switch (a.group) {
+    case 1: return launch_tc_g<T, D, 1>(a, km, vm, s);
+    case 2: return launch_tc_g<T, D, 2>(a, km, vm, s);
+    case 4: return launch_tc_g<T, D, 4>(a, km, vm, s);
+    case 8: return launch_tc_g<T, D, 8>(a, km, vm, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+static cudaError_t launch_tc_t(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
+  return a.head_dim == 64 ? launch_tc_d<T, 64>(a, km, vm, s) : launch_tc_d<T, 128>(a, km, vm, s);
+}
+
+cudaError_t launch_decode_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches) {
+  if (a.rows == 0) return cudaSuccess;
+  CUtensorMap km, vm;
+  if (!encode_pool_map(&km, a.k_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim) ||
+      !encode_pool_map(&vm, a.v_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim))
+    return cudaErrorInvalidValue;
+  cudaError_t e = dt == PA_BF16 ? launch_tc_t<__nv_bfloat16>(a, km, vm, s) : launch_tc_t<__half>(a, km, vm, s);
+  ++*launches;
+  return e;
+}
+
+}  // namespace pa

@@ -6,7 +6,8 @@
 //   out = sum_p acc_p 2^(m_p - M) / sum_p l_p 2^(m_p - M).
 // This is the correction step of the single-pass softmax (JuliaPagedAttn README, "Online
 // Softmax") applied to whole partitions instead of single tokens.  Partitions with l_p = 0 hold no
-// token and are skipped; a row with none left is written as zeros.
+// token and are skipped; a row with none left is written as zeros.  A NaN anywhere in a partition
+// propagates to the output, as it does in the two-pass definition.
 //
 // One warp per output row; lanes own head_dim / 32 consecutive elements.
 #include "pa_common.cuh"
@@ -33,7 +34,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
   const float* pl = a.part_l + row * a.n_parts;
   float M = -INFINITY;
   for (int p = lane; p < parts; p += 32)
-    if (pl[p] > 0.f) M = fmaxf(M, pm[p]);
+    if (pl[p] != 0.f) M = fmaxf(M, pm[p]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float L = 0.f;
@@ -44,14 +45,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
     const float* pa_ = a.part_acc + row * a.n_parts * (int64_t)D + lane * kPer;
     for (int p = 0; p < parts; ++p) {
       const float lp = pl[p];
-      if (!(lp > 0.f)) continue;
+      if (lp == 0.f) continue;
       const float f = fast_exp2(pm[p] - M);
       L = fmaf(lp, f, L);
 #pragma unroll
       for (int i = 0; i < kPer; ++i) acc[i] = fmaf(pa_[(int64_t)p * D + i], f, acc[i]);
     }
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const float inv = L != 0.f ? 1.f / L : 0.f;
   T* o = static_cast<T*>(a.out) + row * D + lane * kPer;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) o[i] = Elt<T>::from_float(acc[i] * inv);

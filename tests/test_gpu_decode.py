@@ -159,8 +159,12 @@ def _ragged_case(dtype, Hq, Hkv, D, S, lens, seed, NB=None):
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("S", [8, 16, 32])
 @pytest.mark.parametrize("part", [0, 64, "none"])
-def test_decode_shapes_and_partitions(cuda_lib, dtype, D, G, S, part):
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_decode_shapes_and_partitions(cuda_lib, dtype, D, G, S, part, kernel):
+    """kernel 0 = automatic choice (tensor-core path for bf16/fp16 with block_size % 16 == 0),
+    1 = CUDA-core path forced."""
     pa = cuda_lib
+    pa.set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
     Hkv = 2
     lens = [0, 1, S - 1, S, S + 1, 3 * S + 5, 200, 517]  # history before the new token
     case = _ragged_case(dtype, Hkv * G, Hkv, D, S, lens, seed=D * 31 + G * 7 + S)
@@ -174,7 +178,7 @@ def test_decode_shapes_and_partitions(cuda_lib, dtype, D, G, S, part):
     out = run_decode(pa, case, kp=dk, vp=dv, workspace=ws)
     kp1, vp1 = oracle.paged_kv_write(case.k_pool, case.v_pool, case.k_new, case.v_new, case.slot_mapping)
     ref = oracle.paged_decode(case.q, kp1, vp1, case.block_table, case.context_lens, case.scale)
-    assert_close(out, ref, dtype, f"{dtype} D{D} G{G} S{S} part{part}")
+    assert_close(out, ref, dtype, f"{dtype} D{D} G{G} S{S} part{part} kernel{kernel}")
     assert pa.device_error_flags() == 0
 
 
@@ -192,7 +196,7 @@ def test_single_token_context_returns_v_exactly(cuda_lib, dtype):
 def test_empty_context_gives_zeros(cuda_lib):
     pa = cuda_lib
     case = _ragged_case(torch.bfloat16, 8, 2, 64, 16, [5, 9], seed=6)
-    lens = torch.tensor([0, 10], dtype=torch.int32)
+    lens = torch.tensor([0, 9], dtype=torch.int32)  # history only: the new tokens are not written here
     out = run_decode(pa, case, lens=lens).cpu()
     assert torch.equal(out[0].float(), torch.zeros_like(out[0].float()))
     ref = oracle.paged_decode(case.q[1:], case.k_pool, case.v_pool, case.block_table[1:], lens[1:], case.scale)
@@ -222,21 +226,57 @@ def test_paged_read_is_bit_identical_under_block_relabelling(cuda_lib):
 def test_bad_block_id_is_flagged_and_masked(cuda_lib):
     pa = cuda_lib
     case = _ragged_case(torch.float16, 8, 2, 64, 16, [40, 40], seed=9)
+    lens = case.context_lens - 1  # history only: the new tokens are not written here
     table = case.block_table.clone()
     table[0, 1] = case.num_blocks + 1000  # out of range inside sequence 0's context
     out = pa.paged_attention_decode(case.q.cuda(), case.k_pool.cuda(), case.v_pool.cuda(), table.cuda(),
-                                    case.context_lens.cuda(), case.scale).cpu()
+                                    lens.cuda(), case.scale).cpu()
     assert pa.device_error_flags() & pa.PA_DEVERR_BLOCK_ID
     # sequence 1 is unaffected; sequence 0 stays finite (its bad block is skipped)
     assert torch.isfinite(out.float()).all()
-    ref = oracle.paged_decode(case.q[1:], case.k_pool, case.v_pool, case.block_table[1:],
-                              case.context_lens[1:], case.scale)
+    ref = oracle.paged_decode(case.q[1:], case.k_pool, case.v_pool, case.block_table[1:], lens[1:], case.scale)
     assert_close(out[1:], ref, torch.float16)
     pa.set_option(pa.PA_OPT_CHECKED, 1)
     with pytest.raises(pa.PagedAttnError) as ei:
         pa.paged_attention_decode(case.q.cuda(), case.k_pool.cuda(), case.v_pool.cuda(), table.cuda(),
-                                  case.context_lens.cuda(), case.scale)
+                                  lens.cuda(), case.scale)
     assert ei.value.status == pa.PA_ERANGE
+
+
+def test_nan_in_context_propagates_like_the_definition(cuda_lib):
+    """A NaN key inside the context makes the two-pass softmax NaN; the kernel must not drop it."""
+    pa = cuda_lib
+    case = _ragged_case(torch.bfloat16, 8, 2, 64, 16, [100, 100], seed=12)
+    lens = case.context_lens - 1
+    out = run_decode(pa, case, lens=lens).cpu()  # position 100 (unwritten, NaN) is outside both contexts
+    assert torch.isfinite(out.float()).all()
+    out_nan = run_decode(pa, case, lens=lens + 1).cpu()  # now the NaN row is inside both contexts
+    assert torch.isnan(out_nan.float()).all()
+
+
+def test_tensor_core_path_refuses_unsupported_shapes(cuda_lib):
+    pa = cuda_lib
+    pa.set_option(pa.PA_OPT_DECODE_KERNEL, 2)
+    for dtype, S in ((torch.float32, 16), (torch.bfloat16, 8)):
+        case = _ragged_case(dtype, 8, 2, 64, S, [20], seed=13)
+        with pytest.raises(pa.PagedAttnError) as ei:
+            run_decode(pa, case)
+        assert ei.value.status == pa.PA_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_both_kernels_agree_on_the_serving_shape(cuda_lib, kernel):
+    """CUDA-core and tensor-core decode on a reduced serving batch (8 sequences, 512-4096 tokens)."""
+    pa = cuda_lib
+    pa.set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
+    lens = W.llama_context_lens()[:8]
+    case = _ragged_case(torch.bfloat16, 32, 8, 128, 16, [n - 1 for n in lens], seed=14)
+    dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
+    pa.paged_kv_write(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), dk, dv)
+    out = run_decode(pa, case, kp=dk, vp=dv)
+    kp1, vp1 = oracle.paged_kv_write(case.k_pool, case.v_pool, case.k_new, case.v_new, case.slot_mapping)
+    ref = oracle.paged_decode(case.q, kp1, vp1, case.block_table, case.context_lens, case.scale)
+    assert_close(out, ref, torch.bfloat16, f"kernel {kernel}")
 
 
 def test_workspace_too_small_is_rejected(cuda_lib):
