@@ -172,6 +172,36 @@ PA_API int paged_attention_lse_merge(void* out, const float* part_max, const flo
                               const float* part_acc, int64_t rows, int n_parts, int head_dim,
                               pa_dtype dtype, void* stream);
 
+/*
+ * paged_attention_decode_static_scratch — paged_attention_decode for callers that cannot allocate
+ * device memory.  (The pages have no counterpart: this is a property of the library, not of the
+ * method.)
+ *
+ * Who needs it: code that receives only the buffers it was handed and has no way to obtain more
+ * device memory — a plugin or custom-op interface whose host owns the allocator and offers no
+ * scratch, a serving loop that fixes its whole memory plan at start-up and forbids cudaMalloc on
+ * the hot path (cudaMalloc may synchronize the device), or a foreign-language caller that only
+ * holds raw device pointers.  Such callers cannot provide the split-K workspace.
+ *
+ * Arguments and results are exactly those of paged_attention_decode without the workspace pair.
+ * The split-K scratch lives instead in a file-scope device array of PA_STATIC_SCRATCH_BYTES that
+ * every GPU loading this library holds until the process exits.  No call allocates or frees
+ * anything.
+ *   - The first call on a device looks up the array's device address with that device current (a
+ *     one-time host set-up); make that first call before any stream capture.
+ *   - Problems whose split-K scratch (paged_attention_decode_workspace_size) exceeds
+ *     PA_STATIC_SCRATCH_BYTES are rejected with PA_EWORKSPACE before anything is launched.
+ *   - All calls on a device share the one array and it keeps the last call's contents; nothing in
+ *     it needs to start at zero.  Calls whose kernels overlap on the GPU (other streams, other
+ *     threads) race on the array: serialize them on one stream.
+ */
+#define PA_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+PA_API int paged_attention_decode_static_scratch(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                                 const int32_t* block_table, int64_t block_table_stride,
+                                                 const int32_t* context_lens, int batch, int64_t num_blocks,
+                                                 int block_size, float scale, int n_q_heads, int n_kv_heads,
+                                                 int head_dim, pa_dtype dtype, void* stream);
+
 /* Set / get a process-wide option (PA_OPT_*).  pa_set_option returns PA_EINVAL for an unknown option
  * or a bad value. */
 PA_API int pa_set_option(int option, int64_t value);

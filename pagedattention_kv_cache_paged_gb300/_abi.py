@@ -37,6 +37,8 @@ SIGNATURES = {
                                        _i32, _i32, _i32, _i32, _vp]),
     "copy_blocks": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "paged_attention_lse_merge": (_i32, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp]),
+    "paged_attention_decode_static_scratch": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _i64, _i32, _f32,
+                                                     _i32, _i32, _i32, _i32, _vp]),
     "pa_set_option": (_i32, [_i32, _i64]),
     "pa_get_option": (_i64, [_i32]),
     "pa_last_cuda_error": (_i32, []),
@@ -188,6 +190,38 @@ def paged_attention_decode(q, k_pool, v_pool, block_table, context_lens, scale=N
                                     _dev(context_lens, "context_lens", torch.int32), B, NB, S, float(scale),
                                     Hq, Hkv, D, _code(dt), ws_ptr, ws_bytes, _stream(stream))
     _check("paged_attention_decode", st)
+    return out
+
+
+PA_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def paged_attention_decode_static_scratch(q, k_pool, v_pool, block_table, context_lens, scale=None, out=None,
+                                          stream=None):
+    """Decode attention for callers that cannot allocate device memory: same result as
+    :func:`paged_attention_decode`, with the split-K scratch taken from the library's own fixed
+    device array (PA_STATIC_SCRATCH_BYTES per device) instead of a caller workspace.  Calls that
+    overlap on the GPU share that array and race; serialize them on one stream."""
+    lib = load_library()
+    NB, S, Hkv, D = _pool_dims(k_pool, v_pool)
+    if q.dim() != 3 or q.shape[2] != D:
+        raise ValueError("q must be [batch, n_q_heads, head_dim]")
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    if block_table.dim() != 2 or block_table.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_table must be [batch, max_blocks] and context_lens [batch]")
+    if block_table.stride(1) != 1:
+        raise ValueError("block_table rows must be contiguous")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dt = k_pool.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    st = lib.paged_attention_decode_static_scratch(
+        _dev(out, "out", dt), _dev(q, "q", dt), _dev(k_pool, "k_pool", dt), _dev(v_pool, "v_pool", dt),
+        _dev(block_table, "block_table", torch.int32, contiguous=False), int(block_table.stride(0)),
+        _dev(context_lens, "context_lens", torch.int32), B, NB, S, float(scale), Hq, Hkv, D, _code(dt),
+        _stream(stream))
+    _check("paged_attention_decode_static_scratch", st)
     return out
 
 
