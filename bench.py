@@ -213,6 +213,8 @@ def main():
     ap.add_argument("--layers", type=int, default=4, help="independent layer pools rotated over the steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--partition-tokens", type=int, default=0, help="split-K partition length (0 = library default)")
+    ap.add_argument("--decode-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -222,6 +224,8 @@ def main():
     rank, world, local, dist = dist_setup(args.gpus)
     import pagedattention_kv_cache_paged_gb300 as pa
     lib = pa.load_library()
+    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, args.partition_tokens)
+    pa.set_option(pa.PA_OPT_DECODE_KERNEL, args.decode_kernel)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
@@ -340,7 +344,9 @@ def main():
                    "context_tokens": sum(lens), "batch": B,
                    "l2": f"inputs larger than L2: {args.layers} rotating layer pools, "
                          f"{kvb / 1e6:.0f} MB of K/V read per step",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "partition_tokens": args.partition_tokens or 512,
+                   "decode_kernel": ["auto", "cuda-core", "tensor-core"][args.decode_kernel]},
         "pct_hbm_measured": value / peak,
         "pct_hbm_spec_8000": value / 8000.0,
         "decode_tok_s_attention_only": B * world / (LLAMA_LAYERS * ms_per_step * 1e-3),

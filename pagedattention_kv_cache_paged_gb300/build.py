@@ -44,8 +44,18 @@ def _run(cmd):
 
 
 def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) -> str:
+    """Compile stale translation units and link the library.  PAGEDATTN_NVCC_FLAGS (environment)
+    adds compiler flags, e.g. -D overrides of kernel tuning constants; a change of flags rebuilds
+    everything."""
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
+    user_flags = os.environ.get("PAGEDATTN_NVCC_FLAGS", "").split()
+    stamp = os.path.join(BUILD_DIR, "flags.txt")
+    old = open(stamp).read() if os.path.exists(stamp) else None
+    if old != " ".join(user_flags):
+        force = True
+        with open(stamp, "w") as f:
+            f.write(" ".join(user_flags))
     srcs = sources()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "pagedattn.h"))
@@ -59,7 +69,7 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
         stale = (force or ptxas_info or not os.path.exists(obj)
                  or os.path.getmtime(obj) < max(os.path.getmtime(src), newest_header))
         if stale:
-            jobs.append([nvcc, *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj])
+            jobs.append([nvcc, *ARCH, *CFLAGS, *user_flags, *extra, "-c", src, "-o", obj])
     outputs = []
     if jobs:
         with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:

@@ -33,7 +33,21 @@
 
 namespace pa {
 
-constexpr int kTcWarps = 4;
+// Tuning constants (overridable at build time with -D for measurement sweeps).
+#ifndef PA_TC_WARPS
+#define PA_TC_WARPS 4
+#endif
+#ifndef PA_TC_STAGES_128
+#define PA_TC_STAGES_128 3
+#endif
+#ifndef PA_TC_STAGES_64
+#define PA_TC_STAGES_64 6
+#endif
+#ifndef PA_TC_MIN_CTAS
+#define PA_TC_MIN_CTAS 2
+#endif
+
+constexpr int kTcWarps = PA_TC_WARPS;
 constexpr int kTile = 16;          // tokens per tile (one mma k-step of PV)
 constexpr int kHalfBytes = kTile * 128;  // 16 rows x 64 columns x 2 bytes
 
@@ -41,12 +55,13 @@ template <int D>
 struct TcCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;  // K and V
-  static constexpr int kStages = D == 128 ? 3 : 6;               // per warp
+  static constexpr int kStages = D == 128 ? PA_TC_STAGES_128 : PA_TC_STAGES_64;  // per warp
   static constexpr int kSmemBytes = 1024 /*barriers*/ + 1024 /*alignment*/ + kTcWarps * kStages * kStageBytes;
+  static_assert(kTcWarps * kStages * 8 <= 1024, "barriers must fit their 1 KB slot");
 };
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kTcWarps * 32, 2)
+__global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
     decode_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
