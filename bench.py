@@ -345,7 +345,7 @@ def main():
                    "l2": f"inputs larger than L2: {args.layers} rotating layer pools, "
                          f"{kvb / 1e6:.0f} MB of K/V read per step",
                    "parallelism": f"replicas x{world}",
-                   "partition_tokens": args.partition_tokens or 512,
+                   "partition_tokens": args.partition_tokens or 1024,
                    "decode_kernel": ["auto", "cuda-core", "tensor-core"][args.decode_kernel]},
         "pct_hbm_measured": value / peak,
         "pct_hbm_spec_8000": value / 8000.0,

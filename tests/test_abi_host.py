@@ -83,11 +83,11 @@ def test_workspace_size_follows_the_partition_plan(lib):
     f = lib.paged_attention_decode_workspace_size
     # short tables never split
     assert f(64, 8, 16, 32, 8, 128) == 0
-    # 4096-token tables at the default 512-token partitions: 8 partitions of (128 + 2) floats
+    # 4096-token tables at the default 1024-token partitions: 4 partitions of (128 + 2) floats
     ws = f(64, 256, 16, 32, 8, 128)
-    assert ws >= 64 * 32 * 8 * 130 * 4
+    assert ws >= 64 * 32 * 4 * 130 * 4
     assert ws % 16 == 0
-    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 1024) == 0
+    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 2048) == 0
     assert f(64, 256, 16, 32, 8, 128) < ws
     assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 0) == 0
 
