@@ -204,6 +204,96 @@ def run_reference(args):
     return 0
 
 
+def prefill_flops(case) -> float:
+    """Unmasked (query, key) pairs x 4 x head_dim x query heads (QK^T and PV, 2 flops per MAC)."""
+    qsl = case.query_start_loc.tolist()
+    lens = case.context_lens.tolist()
+    pairs = 0
+    for b in range(len(lens)):
+        m = qsl[b + 1] - qsl[b]
+        n = lens[b]
+        pairs += m * (n - m) + m * (m + 1) // 2
+    return 4.0 * case.head_dim * case.n_q_heads * pairs
+
+
+def run_prefill(args):
+    """Chunked-prefill workload: 128 sequences over a 1024-token shared prefix, suffixes U[0,512],
+    chunks of 256 queries; one step = paged_kv_write of the 32,768 chunk tokens + causal prefill."""
+    import pagedattention_kv_cache_paged_gb300 as pa
+    lib = pa.load_library()
+    pa.set_option(pa.PA_OPT_PREFILL_KERNEL, args.prefill_kernel)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    case = W.prefill_cow()
+    kp, vp = case.k_pool.to(dev), case.v_pool.to(dev)
+    q, kn, vn = case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev)
+    slot, table = case.slot_mapping.to(dev), case.block_table.to(dev)
+    ctx, qsl = case.context_lens.to(dev), case.query_start_loc.to(dev)
+    out = torch.empty_like(q)
+    NB, S, Hkv, Dh = kp.shape
+    T = int(slot.numel())
+    flops = prefill_flops(case)
+
+    def step():
+        st = lib.paged_kv_write(kn.data_ptr(), vn.data_ptr(), slot.data_ptr(), T, kp.data_ptr(), vp.data_ptr(),
+                                NB, S, Hkv, Dh, pa.PA_BF16, sp)
+        if st:
+            raise RuntimeError(f"paged_kv_write status {st}")
+        ev[0].record(stream)
+        st = lib.paged_attention_prefill(out.data_ptr(), q.data_ptr(), qsl.data_ptr(), q.shape[0], kp.data_ptr(),
+                                         vp.data_ptr(), table.data_ptr(), table.stride(0), ctx.data_ptr(),
+                                         ctx.numel(), NB, S, case.scale, case.n_q_heads, Hkv, Dh, pa.PA_BF16, sp)
+        if st:
+            raise RuntimeError(f"paged_attention_prefill status {st}")
+        ev[1].record(stream)
+
+    ev = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+    for _ in range(args.warmup):
+        step()
+    K = args.steps
+    pf_ms = []
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    torch.cuda.synchronize()
+    launches0 = pa.launch_count()
+    clocks.start()
+    ev0.record(stream)
+    for _ in range(K):
+        step()
+        torch.cuda.synchronize()
+        pf_ms.append(ev[0].elapsed_time(ev[1]))
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    launches = pa.launch_count() - launches0
+    total_ms = ev0.elapsed_time(ev1)
+    pf = statistics.median(pf_ms)
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {"bf16_tflops": 1900.0}
+    peak = float(peaks["bf16_tflops"])
+    if pa.device_error_flags() != 0:
+        raise RuntimeError("device error word set during the benchmark")
+    line = {
+        "metric": "paged chunked prefill: TFLOP/s over unmasked pairs", "value": flops / (pf * 1e-3) / 1e12,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V, bf16)",
+        "config": {"workload": "chunked prefill: 128 seqs, 1024-token shared prefix (32 blocks of 32, refcount "
+                               "128), suffix U[0,512], causal chunk of 256, 32q/8kv heads, head_dim 128",
+                   "prefill_kernel": ["auto", "cuda-core", "tensor-core"][args.prefill_kernel],
+                   "gflop_per_step": flops / 1e9, "steps_synchronised": True},
+        "kernel_us": {"prefill_median": pf * 1e3, "step_incl_write": total_ms / K * 1e3},
+        "roofline": {"bound": "tensor", "kernel": "paged_attention_prefill", "achieved": flops / (pf * 1e-3) / 1e12,
+                     "peak": peak, "peak_kind": "measured bf16 dense (burst)", "unit": "TFLOP/s",
+                     "frac": flops / (pf * 1e-3) / 1e12 / peak, "traffic": None},
+        "gpu_launches": launches, "clocks": clk,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -215,9 +305,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--partition-tokens", type=int, default=0, help="split-K partition length (0 = library default)")
     ap.add_argument("--decode-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
+    ap.add_argument("--prefill-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "prefill":
+        return run_prefill(args)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 

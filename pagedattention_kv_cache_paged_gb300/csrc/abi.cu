@@ -356,7 +356,10 @@ int paged_attention_prefill(void* out, const void* q, const int32_t* query_start
       if (m < 0 || m > lens[(size_t)b]) return PA_ERANGE;
     }
   }
-  if (g_options[PA_OPT_PREFILL_KERNEL].load() == 2) return PA_EUNSUPPORTED;
+  const int64_t kernel_opt = g_options[PA_OPT_PREFILL_KERNEL].load();
+  const bool tc_ok = prefill_tc_supported(dtype, block_size, head_dim, n_q_heads / n_kv_heads, num_blocks);
+  if (kernel_opt == 2 && !tc_ok) return PA_EUNSUPPORTED;
+  const bool use_tc = kernel_opt == 2 || (kernel_opt == 0 && tc_ok);
   AttnArgs a{};
   a.out = out;
   a.q = q;
@@ -380,7 +383,7 @@ int paged_attention_prefill(void* out, const void* q, const int32_t* query_start
   a.max_parts = 1;
   a.err = err;
   int launches = 0;
-  cudaError_t e = launch_attn_simt(a, dtype, s, &launches);
+  cudaError_t e = use_tc ? launch_prefill_tc(a, dtype, s, &launches) : launch_attn_simt(a, dtype, s, &launches);
   return finish(e, launches);
 }
 

@@ -90,4 +90,8 @@ cudaError_t launch_lse_merge(const MergeArgs& a, pa_dtype dt, cudaStream_t s, in
 bool decode_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks);
 cudaError_t launch_decode_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
 
+// Tensor-core causal prefill (TMA ring + mma.sync) for bf16/fp16 pools with block_size % 16 == 0.
+bool prefill_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks);
+cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
+
 }  // namespace pa

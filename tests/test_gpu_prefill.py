@@ -56,18 +56,20 @@ def oracle_pools(case):
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 4, 8])
 @pytest.mark.parametrize("S", [16, 32])
-def test_prefill_ragged_chunks(cuda_lib, dtype, D, G, S):
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_prefill_ragged_chunks(cuda_lib, dtype, D, G, S, kernel):
+    """kernel 0 = automatic (tensor-core path for bf16/fp16), 1 = CUDA-core path forced."""
     pa = cuda_lib
-    case = W.varlen_prefill(D + G + S, hist_lens=[0, 5, 40, 17, 130, 0], chunk_lens=[9, 0, 23, 1, 70, 64],
+    case = W.varlen_prefill(D + G + S, hist_lens=[0, 5, 40, 17, 130, 0, 300], chunk_lens=[9, 0, 23, 1, 70, 64, 200],
                             block_size=S, n_q_heads=2 * G, n_kv_heads=2, head_dim=D, dtype=dtype,
-                            num_blocks=64)
-    out, _, _ = run_case(pa, case)
+                            num_blocks=96)
+    out, _, _ = run_case(pa, case, kernel=kernel)
     kp, vp = oracle_pools(case)
     res = oracle.paged_prefill(case.q, case.query_start_loc, kp, vp, case.block_table, case.context_lens,
                                case.scale)
     idx = sorted(res)
     assert len(idx) == case.q.shape[0]
-    assert_close(out[idx], np.stack([res[i] for i in idx]), dtype, f"prefill {dtype} D{D} G{G} S{S}")
+    assert_close(out[idx], np.stack([res[i] for i in idx]), dtype, f"prefill {dtype} D{D} G{G} S{S} k{kernel}")
     assert pa.device_error_flags() == 0
 
 
@@ -106,6 +108,36 @@ def test_prefill_cow_arm_small_equals_unshared_copy(cuda_lib):
     assert torch.equal(bits(out), bits(out2))
 
 
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_prefill_bad_block_id_is_flagged(cuda_lib, kernel):
+    pa = cuda_lib
+    case = W.varlen_prefill(4, hist_lens=[40, 40], chunk_lens=[24, 24], block_size=16, n_q_heads=8, n_kv_heads=2,
+                            head_dim=128, dtype=torch.bfloat16, num_blocks=16)
+    table = case.block_table.clone()
+    table[0, 1] = 999
+    pa.set_option(pa.PA_OPT_PREFILL_KERNEL, kernel)
+    dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
+    pa.paged_kv_write(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), dk, dv)
+    out = pa.paged_attention_prefill(case.q.cuda(), case.query_start_loc.cuda(), dk, dv, table.cuda(),
+                                     case.context_lens.cuda(), case.scale).cpu()
+    assert pa.device_error_flags() & pa.PA_DEVERR_BLOCK_ID
+    kp, vp = oracle_pools(case)
+    res = oracle.paged_prefill(case.q, case.query_start_loc, kp, vp, case.block_table, case.context_lens,
+                               case.scale, seqs=[1])
+    idx = sorted(res)
+    assert_close(out[idx], np.stack([res[i] for i in idx]), torch.bfloat16, "unaffected sequence")
+
+
+def test_prefill_tensor_core_refuses_unsupported(cuda_lib):
+    pa = cuda_lib
+    pa.set_option(pa.PA_OPT_PREFILL_KERNEL, 2)
+    case = W.varlen_prefill(5, hist_lens=[3], chunk_lens=[5], block_size=8, n_q_heads=4, n_kv_heads=2,
+                            head_dim=64, dtype=torch.bfloat16, num_blocks=4)
+    with pytest.raises(pa.PagedAttnError) as ei:
+        run_case(pa, case, kernel=2)
+    assert ei.value.status == pa.PA_EUNSUPPORTED
+
+
 def test_prefill_bad_query_start_loc_is_flagged(cuda_lib):
     pa = cuda_lib
     case = W.varlen_prefill(3, hist_lens=[4, 4], chunk_lens=[8, 8], block_size=16, n_q_heads=8, n_kv_heads=2,
@@ -135,11 +167,13 @@ def _sampled_check(case, out, seqs, rows_per_seq):
 
 
 @pytest.mark.slow
-def test_prefill_shared_prefix_full(cuda_lib):
-    """Chunked prefill, 128 sequences over a 1024-token shared prefix: sampled rows vs the oracle."""
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_prefill_shared_prefix_full(cuda_lib, kernel):
+    """Chunked prefill, 128 sequences over a 1024-token shared prefix: sampled rows vs the oracle
+    (kernel 1 = CUDA-core, 2 = tensor-core, the launch configuration bench.py times)."""
     pa = cuda_lib
     case = W.prefill_cow()
-    out, _, _ = run_case(pa, case)
+    out, _, _ = run_case(pa, case, kernel=kernel)
     assert torch.isfinite(out.float()).all()
     _sampled_check(case, out, seqs=[0, 1, 37, 64, 100, 127], rows_per_seq=16)
 
