@@ -44,8 +44,17 @@ struct PfCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kOperandBytes = kSub * kHalves * kBoxBytes;  // one of K or V per stage
   static constexpr int kStageBytes = 2 * kOperandBytes;
-  static constexpr int kSmemBytes = 1024 + 1024 + kPfStages * kStageBytes;
+  static constexpr int kQBytes = kPfRows * D * 2;                  // Q rows of the CTA, swizzled
+  static constexpr int kSmemBytes = 1024 + 1024 + kPfStages * kStageBytes + kQBytes;
 };
+
+// Byte offset of (row r, 8-element chunk c) in the CTA's Q block: 16-row groups of head_dim/64
+// swizzled 128-byte halves, laid out like one operand of a K/V stage.
+template <int D>
+__device__ __forceinline__ uint32_t q_offset(int r, int c) {
+  const int grp = r >> 4, rr = r & 15;
+  return (uint32_t)((grp * PfCfg<D>::kHalves + (c >> 3)) * kBoxBytes + rr * 128 + (((c & 7) ^ (rr & 7)) << 4));
+}
 
 // Byte offset of (key kk in 0..63, 8-element chunk c along head_dim) inside one operand of a stage.
 template <int D>
@@ -55,7 +64,7 @@ __device__ __forceinline__ uint32_t pf_offset(int kk, int c) {
 }
 
 template <typename T, int D, int G>
-__global__ void __maxnreg__(224)
+__global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap) {
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -185,22 +194,24 @@ __global__ void __maxnreg__(224)
     tok[i] = T0 + r_lane[i] / G;
     head[i] = kvh * G + r_lane[i] % G;
   }
-  // Q fragments (A operand, rows g and g+8): [ks][0..3]
-  uint32_t qa[kKSteps][4];
-#pragma unroll
-  for (int ks = 0; ks < kKSteps; ++ks) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      uint32_t lo = 0u, hi = 0u;
-      if (tok[i] < T1) {
-        const T* qrow = static_cast<const T*>(a.q) + (tok[i] * a.n_q_heads + head[i]) * D;
-        lo = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig));
-        hi = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig));
+  // Q rows of this warp into shared memory (swizzled), read back as A fragments by ldmatrix
+  uint8_t* qs = stages + kPfStages * kStageBytes;
+  {
+    constexpr int kChunks = D / 8;
+    for (int i = lane; i < 16 * kChunks; i += 32) {
+      const int rr = i / kChunks, c = i % kChunks;
+      const int r = 16 * warp + rr;
+      const int64_t t = T0 + r / G;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t < T1) {
+        const T* qrow = static_cast<const T*>(a.q) + (t * a.n_q_heads + kvh * G + r % G) * D;
+        v = __ldg(reinterpret_cast<const uint4*>(qrow + c * 8));
       }
-      qa[ks][i] = lo;      // a0 (row g) / a1 (row g+8), columns 2tig..
-      qa[ks][2 + i] = hi;  // a2 / a3, columns 8+2tig..
+      *reinterpret_cast<uint4*>(qs + q_offset<D>(r, c)) = v;
     }
+    __syncwarp();
   }
+  const uint32_t qb = smem_u32(qs);
 
   float o[kDTiles][4];
 #pragma unroll
@@ -247,26 +258,34 @@ __global__ void __maxnreg__(224)
         for (int i = lane; i < kKeyTile * 8 * kHalves; i += 32) {
           const int kk = i / (8 * kHalves);
           const int c = i % (8 * kHalves);
-          if (kbase + kk >= sg.n && sub_ok[kk >> 4])
+          const int64_t k0 = kbase + (kk & ~15);
+          if (kbase + kk >= sg.n && k0 < sg.kv_end)
             *reinterpret_cast<uint4*>(st + kOpBytes + pf_offset<D>(kk, c)) = make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
       }
       const uint32_t kb = smem_u32(st);
       const uint32_t vb = smem_u32(st + kOpBytes);
-      // ---- S = Q K^T: 8 n-tiles of 8 keys ---------------------------------------------------
+      // ---- S = Q K^T: 8 n-tiles of 8 keys, k-steps outermost (one Q fragment pair live) -------
       float sc[kKeyTile / 8][4];
 #pragma unroll
-      for (int nt = 0; nt < kKeyTile / 8; ++nt) {
-        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-        if (!sub_ok[nt >> 1]) continue;
-        const int kk = nt * 8 + (lane & 7);
+      for (int nt = 0; nt < kKeyTile / 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < kKSteps; ks += 2) {
+      for (int ks = 0; ks < kKSteps; ks += 2) {
+        uint32_t qf[2][4];
+        const int mi = lane >> 3;
+        const int qr = 16 * warp + (lane & 7) + 8 * (mi & 1);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          ldsm_x4(qb + q_offset<D>(qr, 2 * (ks + j) + (mi >> 1)), qf[j][0], qf[j][1], qf[j][2], qf[j][3]);
+#pragma unroll
+        for (int nt = 0; nt < kKeyTile / 8; ++nt) {
+          if (!sub_ok[nt >> 1]) continue;
+          const int kk = nt * 8 + (lane & 7);
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kb + pf_offset<D>(kk, 2 * ks + (lane >> 3)), b0, b1, b2, b3);
-          mma_16816<kBf16>(sc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-          mma_16816<kBf16>(sc[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
+          mma_16816<kBf16>(sc[nt], qf[0][0], qf[0][1], qf[0][2], qf[0][3], b0, b1);
+          mma_16816<kBf16>(sc[nt], qf[1][0], qf[1][1], qf[1][2], qf[1][3], b2, b3);
         }
       }
       // ---- causal mask, online softmax per row ------------------------------------------------
