@@ -282,7 +282,7 @@ def run_prefill(args):
         "data": "synthetic (seeded N(0,1) Q/K/V, bf16)",
         "config": {"workload": "chunked prefill: 128 seqs, 1024-token shared prefix (32 blocks of 32, refcount "
                                "128), suffix U[0,512], causal chunk of 256, 32q/8kv heads, head_dim 128",
-                   "prefill_kernel": ["auto", "cuda-core", "tensor-core"][args.prefill_kernel],
+                   "prefill_kernel": ["auto (tcgen05)", "cuda-core", "tcgen05", "mma.sync"][args.prefill_kernel],
                    "gflop_per_step": flops / 1e9, "steps_synchronised": True},
         "kernel_us": {"prefill_median": pf * 1e3, "step_incl_write": total_ms / K * 1e3},
         "roofline": {"bound": "tensor", "kernel": "paged_attention_prefill", "achieved": flops / (pf * 1e-3) / 1e12,
@@ -306,7 +306,7 @@ def main():
     ap.add_argument("--partition-tokens", type=int, default=0, help="split-K partition length (0 = library default)")
     ap.add_argument("--decode-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
-    ap.add_argument("--prefill-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--prefill-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05, 3 mma.sync")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -83,7 +83,8 @@ enum {
   PA_OPT_CHECKED = 1,          /* 0 (default) or 1: host-side validation before each launch */
   PA_OPT_DECODE_KERNEL = 2,    /* 0 auto (default), 1 CUDA-core kernel, 2 tensor-core kernel */
   PA_OPT_PARTITION_TOKENS = 3, /* 0 auto (default: 1024) or split-K partition length in tokens, rounded up to block_size */
-  PA_OPT_PREFILL_KERNEL = 4    /* 0 auto (default), 1 CUDA-core kernel, 2 tensor-core kernel */
+  PA_OPT_PREFILL_KERNEL = 4    /* 0 auto (default), 1 CUDA-core kernel, 2 tcgen05 tensor-core kernel,
+                                  3 mma.sync tensor-core kernel */
 };
 
 /*

@@ -148,8 +148,10 @@ int pa_set_option(int option, int64_t value) {
       if (value != 0 && value != 1) return PA_EINVAL;
       break;
     case PA_OPT_DECODE_KERNEL:
-    case PA_OPT_PREFILL_KERNEL:
       if (value < 0 || value > 2) return PA_EINVAL;
+      break;
+    case PA_OPT_PREFILL_KERNEL:
+      if (value < 0 || value > 3) return PA_EINVAL;
       break;
     case PA_OPT_PARTITION_TOKENS:
       if (value < 0 || value > (int64_t(1) << 30)) return PA_EINVAL;
@@ -358,8 +360,9 @@ int paged_attention_prefill(void* out, const void* q, const int32_t* query_start
   }
   const int64_t kernel_opt = g_options[PA_OPT_PREFILL_KERNEL].load();
   const bool tc_ok = prefill_tc_supported(dtype, block_size, head_dim, n_q_heads / n_kv_heads, num_blocks);
-  if (kernel_opt == 2 && !tc_ok) return PA_EUNSUPPORTED;
-  const bool use_tc = kernel_opt == 2 || (kernel_opt == 0 && tc_ok);
+  if ((kernel_opt == 2 || kernel_opt == 3) && !tc_ok) return PA_EUNSUPPORTED;
+  // 0 auto and 2 -> tcgen05 kernel; 3 -> mma.sync kernel; 1 -> CUDA cores
+  const int path = kernel_opt == 1 || !tc_ok ? 1 : (kernel_opt == 3 ? 3 : 2);
   AttnArgs a{};
   a.out = out;
   a.q = q;
@@ -383,7 +386,9 @@ int paged_attention_prefill(void* out, const void* q, const int32_t* query_start
   a.max_parts = 1;
   a.err = err;
   int launches = 0;
-  cudaError_t e = use_tc ? launch_prefill_tc(a, dtype, s, &launches) : launch_attn_simt(a, dtype, s, &launches);
+  cudaError_t e = path == 2   ? launch_prefill_umma(a, dtype, s, &launches)
+                  : path == 3 ? launch_prefill_tc(a, dtype, s, &launches)
+                              : launch_attn_simt(a, dtype, s, &launches);
   return finish(e, launches);
 }
 

@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
 
   for (int j = 0; j < my_tiles; ++j) {
     const int s = j % kStages;
-    if (!mbar_wait(&my_bars[s], (unsigned)((j / kStages) & 1))) {
+    if (!mbar_wait(&my_bars[s], (unsigned)((j / kStages) & 1), a.err)) {
       timed_out = true;
       break;
     }

@@ -94,4 +94,7 @@ cudaError_t launch_decode_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int
 bool prefill_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks);
 cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
 
+// tcgen05 causal prefill (TMEM accumulators, TMA ring, warp-specialised), same support set.
+cudaError_t launch_prefill_umma(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
+
 }  // namespace pa

@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int tile = 0; tile < n_tiles; ++tile, ++it) {
           const int s = it % kPfStages;
           const int round = it / kPfStages;
-          if (round > 0 && !mbar_wait(&empty[s], (unsigned)((round - 1) & 1))) {
+          if (round > 0 && !mbar_wait(&empty[s], (unsigned)((round - 1) & 1), a.err)) {
             raise_error(a.err, PA_DEVERR_TIMEOUT);
             alive = false;
             break;
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int n_tiles = (int)((sg.kv_end + kKeyTile - 1) / kKeyTile);
     for (int tile = 0; tile < n_tiles; ++tile, ++it) {
       const int s = it % kPfStages;
-      if (!mbar_wait(&full[s], (unsigned)((it / kPfStages) & 1))) {
+      if (!mbar_wait(&full[s], (unsigned)((it / kPfStages) & 1), a.err)) {
         if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
         alive = false;
         break;

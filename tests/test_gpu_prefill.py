@@ -56,9 +56,9 @@ def oracle_pools(case):
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 4, 8])
 @pytest.mark.parametrize("S", [16, 32])
-@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("kernel", [0, 1, 3])
 def test_prefill_ragged_chunks(cuda_lib, dtype, D, G, S, kernel):
-    """kernel 0 = automatic (tensor-core path for bf16/fp16), 1 = CUDA-core path forced."""
+    """kernel 0 = automatic (tcgen05 path for bf16/fp16), 1 = CUDA cores, 3 = mma.sync path."""
     pa = cuda_lib
     case = W.varlen_prefill(D + G + S, hist_lens=[0, 5, 40, 17, 130, 0, 300], chunk_lens=[9, 0, 23, 1, 70, 64, 200],
                             block_size=S, n_q_heads=2 * G, n_kv_heads=2, head_dim=D, dtype=dtype,
@@ -73,7 +73,8 @@ def test_prefill_ragged_chunks(cuda_lib, dtype, D, G, S, kernel):
     assert pa.device_error_flags() == 0
 
 
-def test_prefill_cow_arm_small_equals_unshared_copy(cuda_lib):
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_prefill_cow_arm_small_equals_unshared_copy(cuda_lib, kernel):
     """Copy-on-write fork of a shared partial block: the forked sequences attend exactly like
     sequences that never shared (JuliaPagedAttn README, "Copy-on-Write")."""
     pa = cuda_lib
@@ -81,7 +82,7 @@ def test_prefill_cow_arm_small_equals_unshared_copy(cuda_lib):
                            n_kv_heads=8, head_dim=128, dtype=torch.bfloat16, num_blocks=80,
                            suffix_in_cache=False)
     assert case.copy_pairs.shape[0] == 5
-    out, _, _ = run_case(pa, case)
+    out, _, _ = run_case(pa, case, kernel=kernel)
     qsl = case.query_start_loc.tolist()
     for b in range(6):
         k_l, v_l = case.extra["logical"][b]
@@ -108,7 +109,7 @@ def test_prefill_cow_arm_small_equals_unshared_copy(cuda_lib):
     assert torch.equal(bits(out), bits(out2))
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_prefill_bad_block_id_is_flagged(cuda_lib, kernel):
     pa = cuda_lib
     case = W.varlen_prefill(4, hist_lens=[40, 40], chunk_lens=[24, 24], block_size=16, n_q_heads=8, n_kv_heads=2,
@@ -167,10 +168,10 @@ def _sampled_check(case, out, seqs, rows_per_seq):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_prefill_shared_prefix_full(cuda_lib, kernel):
     """Chunked prefill, 128 sequences over a 1024-token shared prefix: sampled rows vs the oracle
-    (kernel 1 = CUDA-core, 2 = tensor-core, the launch configuration bench.py times)."""
+    (kernel 1 = CUDA cores, 2 = tcgen05 (the launch configuration bench.py times), 3 = mma.sync)."""
     pa = cuda_lib
     case = W.prefill_cow()
     out, _, _ = run_case(pa, case, kernel=kernel)
