@@ -60,6 +60,8 @@ def oracle_pools(case):
 def test_prefill_ragged_chunks(cuda_lib, dtype, D, G, S, kernel):
     """kernel 0 = automatic (tcgen05 path for bf16/fp16), 1 = CUDA cores, 3 = mma.sync path."""
     pa = cuda_lib
+    if kernel == 3 and dtype == torch.float32:
+        pytest.skip("the tensor-core paths take bf16/fp16 only (fp32 is covered by kernels 0 and 1)")
     case = W.varlen_prefill(D + G + S, hist_lens=[0, 5, 40, 17, 130, 0, 300], chunk_lens=[9, 0, 23, 1, 70, 64, 200],
                             block_size=S, n_q_heads=2 * G, n_kv_heads=2, head_dim=D, dtype=dtype,
                             num_blocks=96)
