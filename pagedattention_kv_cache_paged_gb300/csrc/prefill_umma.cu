@@ -5,18 +5,22 @@
 // positions of sequence b's context and query r attends to positions 0 .. n_b - m_b + r through
 // the block table — on the 5th-generation tensor cores with accumulators in tensor memory.
 //
-// CTA = 128 (query token, head) rows of one KV head (kRows / G tokens x the G heads of the group:
-// read-time GQA, nanoserve Day 19 "What I learned" 4), 6 warps:
-//   warps 0-3  softmax: thread t owns row t = TMEM lane t; loads its Q row to shared memory, turns
-//              each S tile into probabilities, rescales O in TMEM when its running max grows,
-//              writes P (bf16) to shared memory, and normalises O at the end;
-//   warp 4     producer: TMA loads of 128-key K and V tiles (boxes of 16 keys x 64 columns from the
-//              physical blocks the table names) into a 2-stage ring;
-//   warp 5     MMA: allocates TMEM (S: 128 columns, O: head_dim columns) and issues
-//              S = Q K^T (M 128, N 128) and O += P V (M 128, N head_dim, V as an MN-major operand)
-//              with tcgen05.mma, signalling completion through tcgen05.commit.
-// Handoffs: kv_full/kv_empty (producer <-> MMA), s_full (MMA -> softmax), p_full (softmax -> MMA),
-// pv_done (MMA -> softmax).  Every wait is bounded (PA_DEVERR_TIMEOUT); TMEM is always released.
+// CTA = 256 (query token, head) rows of one KV head, split into two 128-row Q tiles that share
+// every K/V tile (kRows / G tokens x the G heads of the group: read-time GQA, nanoserve Day 19
+// "What I learned" 4).  10 warps:
+//   warps 0-3 / 4-7  softmax groups 0 / 1: thread t of group k owns row 128k + t (TMEM lane t of
+//              S_k and O_k); stages its Q row, turns each S_k tile into probabilities, rescales O_k
+//              in TMEM only when its stabilising maximum has to move up by more than 2^8, writes
+//              P_k (bf16/fp16) to shared memory, and normalises O_k at the end;
+//   warp 8     producer: lane 0 streams 64-key K tiles, lane 1 the matching V tiles (TMA boxes of
+//              16 keys x 64 columns from the physical blocks the table names) into 2-stage rings;
+//   warp 9     MMA: allocates TMEM (S_0, S_1: 64 columns each; O_0, O_1: head_dim each) and
+//              issues S_k = Q_k K^T (M 128, N 64) and O_k += P_k V (M 128, N head_dim, V as an
+//              MN-major operand) with tcgen05.mma, ordered so that the tensor core works on one
+//              group's products while the other group computes its softmax.
+// Every mbarrier wait is bounded (PA_DEVERR_TIMEOUT, with a cooperative abort); TMEM is always
+// released.  The stabilising maximum is exact bookkeeping: numerator and denominator use the
+// same one, so the result equals the running-max form of "Online Softmax" in real arithmetic.
 #include <cudaTypedefs.h>
 
 #include "pa_common.cuh"
@@ -25,53 +29,56 @@
 
 namespace pa {
 
-constexpr int kUmThreads = 192;
-constexpr int kUmRows = 128;   // M of both products
-constexpr int kUmKeys = 128;   // keys per tile
+constexpr int kUmThreads = 320;
+constexpr int kUmTileRows = 128;            // rows per Q tile (MMA M)
+constexpr int kUmRows = 2 * kUmTileRows;    // rows per CTA
+constexpr int kUmKeys = 64;                 // keys per K/V tile (N of S, K of PV)
 constexpr int kUmSub = kUmKeys / 16;
-constexpr int kUmStages = 2;
-constexpr int kUmTmemCols = 256;
-constexpr int kUmHalf = 128 * 128;  // bytes of one 64-column half of a 128-row operand
+constexpr int kUmTmemCols = 512;
+constexpr float kUmRescaleThreshold = 8.f;  // log2 units: O is rescaled when the max grows by > 2^8
 
 template <int D>
 struct UmCfg {
   static constexpr int kHalves = D / 64;
-  static constexpr int kOpBytes = kUmKeys * D * 2;
-  static constexpr int kStageBytes = 2 * kOpBytes;
-  static constexpr int kQBytes = kUmRows * D * 2;
-  static constexpr int kPBytes = kUmRows * kUmKeys * 2;
-  static constexpr int kSmemBytes = 1024 + 1024 + kUmStages * kStageBytes + kQBytes + kPBytes;
+  static constexpr int kQHalf = kUmTileRows * 128;   // one 64-column half of a Q tile
+  static constexpr int kQBytes = kUmTileRows * D * 2;
+  static constexpr int kKvHalf = kUmKeys * 128;      // one 64-column half of a K or V tile
+  static constexpr int kKvBytes = kUmKeys * D * 2;
+  static constexpr int kPBytes = kUmTileRows * kUmKeys * 2;
+  static constexpr int kSmemBytes = 1024 + 1024 + 2 * kQBytes + 4 * kKvBytes + 2 * kPBytes;
 };
 
-// Byte offset of (row r in 0..127, 8-element chunk c) in a [half][row][128 B] swizzled operand.
-__device__ __forceinline__ uint32_t um_off(int r, int c) {
-  return (uint32_t)((c >> 3) * kUmHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// Byte offset of (row r, 8-element chunk c) in a [half][rows][128 B] swizzled operand.
+__device__ __forceinline__ uint32_t sw_off(int r, int c, int half_bytes) {
+  return (uint32_t)((c >> 3) * half_bytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kUmThreads, 1)
     prefill_umma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
+  using Cfg = UmCfg<D>;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-  constexpr int kHalves = UmCfg<D>::kHalves;
-  constexpr int kOpBytes = UmCfg<D>::kOpBytes;
-  constexpr int kStageBytes = UmCfg<D>::kStageBytes;
+  constexpr int kHalves = Cfg::kHalves;
   constexpr int kQB = kUmRows / G;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base);
-  uint64_t* kv_full = bars;       // [2]
-  uint64_t* kv_empty = bars + 2;  // [2]
-  uint64_t* q_ready = bars + 4;
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* pv_done = bars + 7;
-  uint64_t* fin = bars + 8;
+  uint64_t* kfull = bars + 0;     // [2]
+  uint64_t* kempty = bars + 2;    // [2]
+  uint64_t* vfull = bars + 4;     // [2]
+  uint64_t* vempty = bars + 6;    // [2]
+  uint64_t* q_ready = bars + 8;
+  uint64_t* s_full = bars + 9;    // [2] per group
+  uint64_t* p_full = bars + 11;   // [2]
+  uint64_t* pv_done = bars + 13;  // [2]
+  uint64_t* fin = bars + 15;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 512);
-  uint8_t* stages = base + 1024;
-  uint8_t* qs = stages + kUmStages * kStageBytes;
-  uint8_t* ps = qs + UmCfg<D>::kQBytes;
+  uint8_t* qs = base + 1024;                       // [2][Q tile]
+  uint8_t* ks = qs + 2 * Cfg::kQBytes;             // [2 stages][K tile]
+  uint8_t* vs = ks + 2 * Cfg::kKvBytes;            // [2 stages][V tile]
+  uint8_t* ps = vs + 2 * Cfg::kKvBytes;            // [2 groups][P tile]
 
   const int kvh = blockIdx.x % a.n_kv_heads;
   const int64_t T0 = (int64_t)(blockIdx.x / a.n_kv_heads) * kQB;
@@ -84,25 +91,28 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   if (threadIdx.x == 0) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
-    mbar_init(&kv_full[0], 1);
-    mbar_init(&kv_full[1], 1);
-    mbar_init(&kv_empty[0], 1);
-    mbar_init(&kv_empty[1], 1);
-    mbar_init(q_ready, 128);
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 128);
+      mbar_init(&pv_done[s], 1);
+    }
+    mbar_init(q_ready, 256);
     mbar_init(fin, 1);
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 5) tmem_alloc(tmem_slot, kUmTmemCols);
+  if (warp == 9) tmem_alloc(tmem_slot, kUmTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;
-  const uint32_t tO = tmem + 128;
+  // S_k at columns [64k, 64k + 64), O_k at [128 + 128k, 128 + 128k + D)
+  auto tS = [&](int k) { return tmem + 64u * (uint32_t)k; };
+  auto tO = [&](int k) { return tmem + 128u + 128u * (uint32_t)k; };
 
   struct Seg {
     int b;
@@ -128,9 +138,14 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   };
   auto tiles_of = [](const Seg& sg) -> int { return (int)((sg.kv_end + kUmKeys - 1) / kUmKeys); };
 
-  if (warp == 4) {
-    // --------------------------------------- producer -------------------------------------------
-    if (lane == 0) {
+  if (warp == 8) {
+    // --------------------------- producer: lane 0 -> K tiles, lane 1 -> V tiles --------------------
+    if (lane < 2) {
+      const bool is_v = lane == 1;
+      uint64_t* full = is_v ? vfull : kfull;
+      uint64_t* empty = is_v ? vempty : kempty;
+      uint8_t* ring = is_v ? vs : ks;
+      const CUtensorMap* map = is_v ? &vmap : &kmap;
       int i = 0;
       bool alive = true;
       for (int64_t t = T0; t < T1 && alive;) {
@@ -139,7 +154,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         const int nt = tiles_of(sg);
         for (int tile = 0; tile < nt; ++tile, ++i) {
           const int s = i & 1;
-          if (i >= 2 && !mbar_wait(&kv_empty[s], (unsigned)(((i >> 1) - 1) & 1), a.err)) {
+          if (i >= 2 && !mbar_wait(&empty[s], (unsigned)(((i >> 1) - 1) & 1), a.err)) {
             raise_error(a.err, PA_DEVERR_TIMEOUT);
             alive = false;
             break;
@@ -153,34 +168,31 @@ __global__ void __launch_bounds__(kUmThreads, 1)
             if (k0 < sg.kv_end) {
               const int blk = __ldg(table + (k0 >> a.block_shift));
               if (blk < 0 || blk >= a.num_blocks) {
-                raise_error(a.err, PA_DEVERR_BLOCK_ID);
+                if (!is_v) raise_error(a.err, PA_DEVERR_BLOCK_ID);
               } else {
                 ys[sub] = (int)(((int64_t)blk << a.block_shift) + (k0 & bmask));
-                bytes += 2 * kHalves * 2048;
+                bytes += kHalves * 2048;
               }
             }
           }
-          uint8_t* st = stages + s * kStageBytes;
+          uint8_t* st = ring + s * Cfg::kKvBytes;
           if (bytes == 0) {
-            mbar_arrive(&kv_full[s]);
+            mbar_arrive(&full[s]);
           } else {
-            mbar_arrive_expect_tx(&kv_full[s], bytes);
+            mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
             for (int sub = 0; sub < kUmSub; ++sub) {
               if (ys[sub] < 0) continue;
 #pragma unroll
-              for (int h = 0; h < kHalves; ++h) {
-                const int off = h * kUmHalf + sub * 2048;
-                tma_load_2d(st + off, &kmap, kvh * D + h * 64, ys[sub], &kv_full[s]);
-                tma_load_2d(st + kOpBytes + off, &vmap, kvh * D + h * 64, ys[sub], &kv_full[s]);
-              }
+              for (int h = 0; h < kHalves; ++h)
+                tma_load_2d(st + h * Cfg::kKvHalf + sub * 2048, map, kvh * D + h * 64, ys[sub], &full[s]);
             }
           }
         }
         t = sg.seg1;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------ MMA ---------------------------------------------
     if (lane == 0) {
       int n_all = 0;
@@ -191,84 +203,105 @@ __global__ void __launch_bounds__(kUmThreads, 1)
       }
       const uint32_t id_s = umma_idesc_f16(kBf16, 128, kUmKeys, false, false);
       const uint32_t id_pv = umma_idesc_f16(kBf16, 128, D, false, true);
-      const uint32_t q_addr = smem_u32(qs), p_addr = smem_u32(ps);
-      auto issue_s = [&](int i) {
-        const uint32_t k_addr = smem_u32(stages + (i & 1) * kStageBytes);
+      auto issue_s = [&](int k, int i) {
+        const uint32_t qa = smem_u32(qs + k * Cfg::kQBytes);
+        const uint32_t ka = smem_u32(ks + (i & 1) * Cfg::kKvBytes);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kUmHalf + (ks & 3) * 32;
-          umma_ss(tS, umma_desc_sw128(q_addr + off, 16, 1024), umma_desc_sw128(k_addr + off, 16, 1024), id_s,
-                  ks > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qo = (kk >> 2) * Cfg::kQHalf + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * Cfg::kKvHalf + (kk & 3) * 32;
+          umma_ss(tS(k), umma_desc_sw128(qa + qo, 16, 1024), umma_desc_sw128(ka + ko, 16, 1024), id_s,
+                  kk > 0 ? 1u : 0u);
         }
-        umma_commit(s_full);
+        umma_commit(&s_full[k]);
+      };
+      auto issue_pv = [&](int k, int i) {
+        const uint32_t pa_ = smem_u32(ps + k * Cfg::kPBytes);
+        const uint32_t va = smem_u32(vs + (i & 1) * Cfg::kKvBytes);
+#pragma unroll
+        for (int kk = 0; kk < kUmKeys / 16; ++kk)
+          umma_ss(tO(k), umma_desc_sw128(pa_ + kk * 32, 16, 1024),
+                  umma_desc_sw128(va + kk * 2048, Cfg::kKvHalf, 1024), id_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&pv_done[k]);
       };
       bool alive = mbar_wait(q_ready, 0, a.err);
       if (alive && n_all > 0) {
-        alive = mbar_wait(&kv_full[0], 0, a.err);
+        alive = mbar_wait(&kfull[0], 0, a.err);
         if (alive) {
           tc_fence_after();
-          issue_s(0);
+          issue_s(0, 0);
+          issue_s(1, 0);
+          umma_commit(&kempty[0]);
         }
       }
       for (int i = 0; i < n_all && alive; ++i) {
-        if (!mbar_wait(p_full, (unsigned)(i & 1), a.err)) {
+        const bool more = i + 1 < n_all;
+        if (!mbar_wait(&vfull[i & 1], (unsigned)((i >> 1) & 1), a.err) ||
+            !mbar_wait(&p_full[0], (unsigned)(i & 1), a.err)) {
           alive = false;
           break;
         }
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(stages + (i & 1) * kStageBytes + kOpBytes);
-#pragma unroll
-        for (int ks = 0; ks < kUmKeys / 16; ++ks) {
-          const uint32_t aoff = (ks >> 2) * kUmHalf + (ks & 3) * 32;
-          umma_ss(tO, umma_desc_sw128(p_addr + aoff, 16, 1024),
-                  umma_desc_sw128(v_addr + ks * 2048, kUmHalf, 1024), id_pv, (i > 0 || ks > 0) ? 1u : 0u);
-        }
-        umma_commit(pv_done);
-        umma_commit(&kv_empty[i & 1]);
-        if (i + 1 < n_all) {
-          if (!mbar_wait(&kv_full[(i + 1) & 1], (unsigned)(((i + 1) >> 1) & 1), a.err)) {
+        issue_pv(0, i);
+        if (more) {
+          if (!mbar_wait(&kfull[(i + 1) & 1], (unsigned)(((i + 1) >> 1) & 1), a.err)) {
             alive = false;
             break;
           }
           tc_fence_after();
-          issue_s(i + 1);
+          issue_s(0, i + 1);
+        }
+        if (!mbar_wait(&p_full[1], (unsigned)(i & 1), a.err)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(1, i);
+        umma_commit(&vempty[i & 1]);
+        if (more) {
+          issue_s(1, i + 1);
+          umma_commit(&kempty[(i + 1) & 1]);
         }
       }
       if (!alive) raise_error(a.err, PA_DEVERR_TIMEOUT);
       if (n_all > 0) {
-        umma_commit(fin);  // every MMA issued above has completed once this phase completes
+        umma_commit(fin);
         mbar_wait(fin, 0, a.err);
       }
     }
   } else {
-    // ---------------------------------------- softmax -------------------------------------------
-    const int r = threadIdx.x;  // row = TMEM lane
-    const int64_t tok = T0 + r / G;
-    const int head = kvh * G + r % G;
+    // --------------------------------------- softmax groups ---------------------------------------
+    const int grp = warp >> 2;           // 0 or 1
+    const int r = threadIdx.x & 127;     // row inside the Q tile = TMEM lane
+    const int row = grp * kUmTileRows + r;
+    const int64_t tok = T0 + row / G;
+    const int head = kvh * G + row % G;
+    uint8_t* q_tile = qs + grp * Cfg::kQBytes;
+    uint8_t* p_tile = ps + grp * Cfg::kPBytes;
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + (tok * a.n_q_heads + head) * D);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         const uint4 v = tok < T1 ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qs + um_off(r, c)) = v;
+        *reinterpret_cast<uint4*>(q_tile + sw_off(r, c, Cfg::kQHalf)) = v;
       }
       fence_proxy_async_smem();
       mbar_arrive(q_ready);
     }
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    float m_run = -INFINITY, l_run = 0.f;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    float m_use = -INFINITY;  // stabilising maximum (log2 domain) the exponentials are taken against
+    float l_run = 0.f;
     int i = 0;
     bool alive = true;
     for (int64_t t = T0; t < T1 && alive;) {
       const Seg sg = segment_at(t);
-      if (!sg.ok && r == 0) raise_error(a.err, PA_DEVERR_QUERY_LOC);
+      if (!sg.ok && threadIdx.x == 0) raise_error(a.err, PA_DEVERR_QUERY_LOC);
       const int32_t* table = a.block_table + (int64_t)sg.b * a.bt_stride;
-      const int64_t seg0 = t;
-      const int64_t bound = (sg.ok && tok >= seg0 && tok < sg.seg1) ? sg.pos0 + (tok - sg.q0) : -1;
+      const int64_t bound = (sg.ok && tok >= t && tok < sg.seg1) ? sg.pos0 + (tok - sg.q0) : -1;
       const int nt = tiles_of(sg);
       for (int tile = 0; tile < nt; ++tile, ++i) {
         const int64_t kb = (int64_t)tile * kUmKeys;
-        unsigned loaded = 0;  // bit per 16-key sub-tile holding data
+        unsigned loaded = 0;
 #pragma unroll
         for (int sub = 0; sub < kUmSub; ++sub) {
           const int64_t k0 = kb + sub * 16;
@@ -277,17 +310,16 @@ __global__ void __launch_bounds__(kUmThreads, 1)
             if (blk >= 0 && blk < a.num_blocks) loaded |= 1u << sub;
           }
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full, (unsigned)(i & 1), a.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], (unsigned)(i & 1), a.err))) {
           alive = false;
           break;
         }
         tc_fence_after();
-        // ---- S row -> masked, scaled scores (log2 domain) ------------------------------------
         float x[kUmKeys];
 #pragma unroll
         for (int c0 = 0; c0 < kUmKeys; c0 += 32) {
           uint32_t v[32];
-          tmem_ld32(tS + lane_base + c0, v);
+          tmem_ld32(tS(grp) + lane_base + c0, v);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[c0 + j] = __uint_as_float(v[j]);
@@ -299,20 +331,23 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           x[c] = keep ? x[c] * a.scale_log2 : -INFINITY;
           mx = fmaxf(mx, x[c]);
         }
-        const float m_new = fmaxf(m_run, mx);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float corr = fast_exp2(m_run - m_use);
-        m_run = m_new;
+        // move the stabiliser only when it must: first finite maximum, or growth beyond 2^8
+        float corr = 1.f;
+        if (mx > m_use + kUmRescaleThreshold || (m_use == -INFINITY && mx != -INFINITY)) {
+          corr = fast_exp2(m_use - mx);  // m_use = -inf -> 0
+          m_use = mx;
+        }
+        const float m_sub = m_use == -INFINITY ? 0.f : m_use;
         float rs = 0.f;
 #pragma unroll
         for (int c = 0; c < kUmKeys; ++c) {
-          x[c] = fast_exp2(x[c] - m_use);
+          x[c] = fast_exp2(x[c] - m_sub);
           rs += x[c];
         }
         l_run = l_run * corr + rs;
-        // ---- wait for the previous P V (O stable, P buffer free), then rescale O -------------------
+        // the previous P V of this group must be done: O stable, P buffer free
         if (i > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (unsigned)((i - 1) & 1), a.err))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[grp], (unsigned)((i - 1) & 1), a.err))) {
             alive = false;
             break;
           }
@@ -321,30 +356,31 @@ __global__ void __launch_bounds__(kUmThreads, 1)
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
               uint32_t v[32];
-              tmem_ld32(tO + lane_base + c0, v);
+              tmem_ld32(tO(grp) + lane_base + c0, v);
               tmem_wait_ld();
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * corr);
-              tmem_st32(tO + lane_base + c0, v);
+              tmem_st32(tO(grp) + lane_base + c0, v);
             }
             tmem_wait_st();
           }
         }
-        // ---- V rows that hold no data or lie past the context become zeros ------------------------
-        if (kb + kUmKeys > sg.n || loaded != (1u << kUmSub) - 1u) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[i & 1], (unsigned)((i >> 1) & 1), a.err))) {
+        // group 0 zeroes V rows that hold no data or lie past the context (group 1's P V is issued
+        // after group 0's, so it sees the zeros too)
+        if (grp == 0 && (kb + kUmKeys > sg.n || loaded != (1u << kUmSub) - 1u)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&vfull[i & 1], (unsigned)((i >> 1) & 1), a.err))) {
             alive = false;
             break;
           }
-          uint8_t* vst = stages + (i & 1) * kStageBytes + kOpBytes;
+          uint8_t* vst = vs + (i & 1) * Cfg::kKvBytes;
           for (int e = r; e < kUmKeys * 8 * kHalves; e += 128) {
             const int key = e / (8 * kHalves);
             const int c = e % (8 * kHalves);
             if (kb + key >= sg.n || !((loaded >> (key >> 4)) & 1u))
-              *reinterpret_cast<uint4*>(vst + um_off(key, c)) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(vst + sw_off(key, c, Cfg::kKvHalf)) = make_uint4(0, 0, 0, 0);
           }
         }
-        // ---- P row (bf16/fp16) into shared memory --------------------------------------------------
+        // P row into shared memory: [row][64 keys] = one 128-byte swizzled row
 #pragma unroll
         for (int c = 0; c < kUmKeys / 8; ++c) {
           uint4 w;
@@ -352,48 +388,46 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           w.y = pack2<kBf16>(x[8 * c + 2], x[8 * c + 3]);
           w.z = pack2<kBf16>(x[8 * c + 4], x[8 * c + 5]);
           w.w = pack2<kBf16>(x[8 * c + 6], x[8 * c + 7]);
-          *reinterpret_cast<uint4*>(ps + um_off(r, c)) = w;
+          *reinterpret_cast<uint4*>(p_tile + sw_off(r, c, kUmTileRows * 128)) = w;
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(p_full);
+        mbar_arrive(&p_full[grp]);
       }
       t = sg.seg1;
     }
     if (!alive && lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
-    // ---- epilogue: O / l for this row ----------------------------------------------------------------
     if (alive && i > 0) {
-      alive = __all_sync(0xffffffffu, mbar_wait(pv_done, (unsigned)((i - 1) & 1), a.err));
+      alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[grp], (unsigned)((i - 1) & 1), a.err));
       tc_fence_after();
     }
-    const float inv = (alive && l_run != 0.f) ? 1.f / l_run : 0.f;
+    const bool have = alive && i > 0 && l_run != 0.f;
+    const float inv = have ? 1.f / l_run : 0.f;
     T* orow = static_cast<T*>(a.out) + (tok * a.n_q_heads + head) * D;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t v[32];
-      tmem_ld32(tO + lane_base + c0, v);
+      tmem_ld32(tO(grp) + lane_base + c0, v);
       tmem_wait_ld();
       if (tok < T1) {
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = have ? __uint_as_float(v[j + e]) * inv : 0.f;
           uint4 w;
-          w.x = pack2<kBf16>(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
-          w.y = pack2<kBf16>(__uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
-          w.z = pack2<kBf16>(__uint_as_float(v[j + 4]) * inv, __uint_as_float(v[j + 5]) * inv);
-          w.w = pack2<kBf16>(__uint_as_float(v[j + 6]) * inv, __uint_as_float(v[j + 7]) * inv);
+          w.x = pack2<kBf16>(f[0], f[1]);
+          w.y = pack2<kBf16>(f[2], f[3]);
+          w.z = pack2<kBf16>(f[4], f[5]);
+          w.w = pack2<kBf16>(f[6], f[7]);
           *reinterpret_cast<uint4*>(orow + c0 + j) = w;
         }
       }
     }
-    // rows that saw no key (l = 0) were never written by P V: O holds no data, write zeros
-    if (tok < T1 && i == 0) {
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
-    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kUmTmemCols);
