@@ -13,11 +13,14 @@
 //              in TMEM only when its stabilising maximum has to move up by more than 2^8, writes
 //              P_k (bf16/fp16) to shared memory, and normalises O_k at the end;
 //   warp 8     producer: lane 0 streams 64-key K tiles, lane 1 the matching V tiles (TMA boxes of
-//              16 keys x 64 columns from the physical blocks the table names) into 2-stage rings;
+//              16 keys x 64 columns from the physical blocks the table names) into a 3-stage K
+//              ring and a 2-stage V ring;
 //   warp 9     MMA: allocates TMEM (S_0, S_1: 64 columns each; O_0, O_1: head_dim each) and
 //              issues S_k = Q_k K^T (M 128, N 64) and O_k += P_k V (M 128, N head_dim, V as an
 //              MN-major operand) with tcgen05.mma, ordered so that the tensor core works on one
-//              group's products while the other group computes its softmax.
+//              group's products while the other group computes its softmax; each group releases its S
+//              as soon as it has been read out of TMEM, so the next S is computed during its
+//              exponentials.
 // Every mbarrier wait is bounded (PA_DEVERR_TIMEOUT, with a cooperative abort); TMEM is always
 // released.  The stabilising maximum is exact bookkeeping: numerator and denominator use the
 // same one, so the result equals the running-max form of "Online Softmax" in real arithmetic.
@@ -35,6 +38,8 @@ constexpr int kUmRows = 2 * kUmTileRows;    // rows per CTA
 constexpr int kUmKeys = 64;                 // keys per K/V tile (N of S, K of PV)
 constexpr int kUmSub = kUmKeys / 16;
 constexpr int kUmTmemCols = 512;
+constexpr int kUmKStages = 3;               // K ring depth (S of the next tile is issued early)
+constexpr int kUmVStages = 2;               // V ring depth
 constexpr float kUmRescaleThreshold = 8.f;  // log2 units: O is rescaled when the max grows by > 2^8
 
 template <int D>
@@ -45,7 +50,7 @@ struct UmCfg {
   static constexpr int kKvHalf = kUmKeys * 128;      // one 64-column half of a K or V tile
   static constexpr int kKvBytes = kUmKeys * D * 2;
   static constexpr int kPBytes = kUmTileRows * kUmKeys * 2;
-  static constexpr int kSmemBytes = 1024 + 1024 + 2 * kQBytes + 4 * kKvBytes + 2 * kPBytes;
+  static constexpr int kSmemBytes = 1024 + 1024 + 2 * kQBytes + (kUmKStages + kUmVStages) * kKvBytes + 2 * kPBytes;
 };
 
 // Byte offset of (row r, 8-element chunk c) in a [half][rows][128 B] swizzled operand.
@@ -65,20 +70,21 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base);
-  uint64_t* kfull = bars + 0;     // [2]
-  uint64_t* kempty = bars + 2;    // [2]
-  uint64_t* vfull = bars + 4;     // [2]
-  uint64_t* vempty = bars + 6;    // [2]
-  uint64_t* q_ready = bars + 8;
-  uint64_t* s_full = bars + 9;    // [2] per group
-  uint64_t* p_full = bars + 11;   // [2]
-  uint64_t* pv_done = bars + 13;  // [2]
-  uint64_t* fin = bars + 15;
+  uint64_t* kfull = bars + 0;     // [3]
+  uint64_t* kempty = bars + 3;    // [3]
+  uint64_t* vfull = bars + 6;     // [2]
+  uint64_t* vempty = bars + 8;    // [2]
+  uint64_t* q_ready = bars + 10;
+  uint64_t* s_full = bars + 11;   // [2] per group: S_k computed
+  uint64_t* s_free = bars + 13;   // [2] per group: S_k read out of TMEM
+  uint64_t* p_full = bars + 15;   // [2] per group: P_k written, O_k rescaled
+  uint64_t* pv_done = bars + 17;  // [2] per group: O_k += P_k V finished
+  uint64_t* fin = bars + 19;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 512);
   uint8_t* qs = base + 1024;                       // [2][Q tile]
-  uint8_t* ks = qs + 2 * Cfg::kQBytes;             // [2 stages][K tile]
-  uint8_t* vs = ks + 2 * Cfg::kKvBytes;            // [2 stages][V tile]
-  uint8_t* ps = vs + 2 * Cfg::kKvBytes;            // [2 groups][P tile]
+  uint8_t* ks = qs + 2 * Cfg::kQBytes;             // [3 stages][K tile]
+  uint8_t* vs = ks + kUmKStages * Cfg::kKvBytes;   // [2 stages][V tile]
+  uint8_t* ps = vs + kUmVStages * Cfg::kKvBytes;   // [2 groups][P tile]
 
   const int kvh = blockIdx.x % a.n_kv_heads;
   const int64_t T0 = (int64_t)(blockIdx.x / a.n_kv_heads) * kQB;
@@ -91,12 +97,15 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   if (threadIdx.x == 0) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kUmKStages; ++s) {
       mbar_init(&kfull[s], 1);
       mbar_init(&kempty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 1);
       mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 128);
       mbar_init(&p_full[s], 128);
       mbar_init(&pv_done[s], 1);
     }
@@ -146,6 +155,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
       uint64_t* empty = is_v ? vempty : kempty;
       uint8_t* ring = is_v ? vs : ks;
       const CUtensorMap* map = is_v ? &vmap : &kmap;
+      const int depth = is_v ? kUmVStages : kUmKStages;
       int i = 0;
       bool alive = true;
       for (int64_t t = T0; t < T1 && alive;) {
@@ -153,8 +163,9 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         const int32_t* table = a.block_table + (int64_t)sg.b * a.bt_stride;
         const int nt = tiles_of(sg);
         for (int tile = 0; tile < nt; ++tile, ++i) {
-          const int s = i & 1;
-          if (i >= 2 && !mbar_wait(&empty[s], (unsigned)(((i >> 1) - 1) & 1), a.err)) {
+          const int s = i % depth;
+          const int round = i / depth;
+          if (round > 0 && !mbar_wait(&empty[s], (unsigned)((round - 1) & 1), a.err)) {
             raise_error(a.err, PA_DEVERR_TIMEOUT);
             alive = false;
             break;
@@ -205,7 +216,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
       const uint32_t id_pv = umma_idesc_f16(kBf16, 128, D, false, true);
       auto issue_s = [&](int k, int i) {
         const uint32_t qa = smem_u32(qs + k * Cfg::kQBytes);
-        const uint32_t ka = smem_u32(ks + (i & 1) * Cfg::kKvBytes);
+        const uint32_t ka = smem_u32(ks + (i % kUmKStages) * Cfg::kKvBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t qo = (kk >> 2) * Cfg::kQHalf + (kk & 3) * 32;
@@ -224,9 +235,12 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                   umma_desc_sw128(va + kk * 2048, Cfg::kKvHalf, 1024), id_pv, (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&pv_done[k]);
       };
+      auto kwait = [&](int j) {
+        return mbar_wait(&kfull[j % kUmKStages], (unsigned)((j / kUmKStages) & 1), a.err);
+      };
       bool alive = mbar_wait(q_ready, 0, a.err);
       if (alive && n_all > 0) {
-        alive = mbar_wait(&kfull[0], 0, a.err);
+        alive = kwait(0);
         if (alive) {
           tc_fence_after();
           issue_s(0, 0);
@@ -235,7 +249,23 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         }
       }
       for (int i = 0; i < n_all && alive; ++i) {
-        const bool more = i + 1 < n_all;
+        // next tile's S products as soon as each group has read its S out of TMEM
+        if (i + 1 < n_all) {
+          if (!kwait(i + 1) || !mbar_wait(&s_free[0], (unsigned)(i & 1), a.err)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(0, i + 1);
+          if (!mbar_wait(&s_free[1], (unsigned)(i & 1), a.err)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(1, i + 1);
+          umma_commit(&kempty[(i + 1) % kUmKStages]);
+        }
+        // this tile's P V products
         if (!mbar_wait(&vfull[i & 1], (unsigned)((i >> 1) & 1), a.err) ||
             !mbar_wait(&p_full[0], (unsigned)(i & 1), a.err)) {
           alive = false;
@@ -243,14 +273,6 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         }
         tc_fence_after();
         issue_pv(0, i);
-        if (more) {
-          if (!mbar_wait(&kfull[(i + 1) & 1], (unsigned)(((i + 1) >> 1) & 1), a.err)) {
-            alive = false;
-            break;
-          }
-          tc_fence_after();
-          issue_s(0, i + 1);
-        }
         if (!mbar_wait(&p_full[1], (unsigned)(i & 1), a.err)) {
           alive = false;
           break;
@@ -258,10 +280,6 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         tc_fence_after();
         issue_pv(1, i);
         umma_commit(&vempty[i & 1]);
-        if (more) {
-          issue_s(1, i + 1);
-          umma_commit(&kempty[(i + 1) & 1]);
-        }
       }
       if (!alive) raise_error(a.err, PA_DEVERR_TIMEOUT);
       if (n_all > 0) {
@@ -324,12 +342,23 @@ __global__ void __launch_bounds__(kUmThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[c0 + j] = __uint_as_float(v[j]);
         }
+        tc_fence_before();
+        mbar_arrive(&s_free[grp]);  // S_k may now be overwritten by the next tile's product
+        // a tile wholly inside this row's causal bound with every sub-tile loaded needs no mask
+        const float sc = a.scale_log2;
+        const bool fast = sc > 0.f && loaded == (1u << kUmSub) - 1u && kb + kUmKeys - 1 <= bound;
         float mx = -INFINITY;
+        if (fast) {
 #pragma unroll
-        for (int c = 0; c < kUmKeys; ++c) {
-          const bool keep = ((loaded >> (c >> 4)) & 1u) && (kb + c <= bound);
-          x[c] = keep ? x[c] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[c]);
+          for (int c = 0; c < kUmKeys; ++c) mx = fmaxf(mx, x[c]);
+          mx *= sc;
+        } else {
+#pragma unroll
+          for (int c = 0; c < kUmKeys; ++c) {
+            const bool keep = ((loaded >> (c >> 4)) & 1u) && (kb + c <= bound);
+            x[c] = keep ? x[c] * sc : -INFINITY;
+            mx = fmaxf(mx, x[c]);
+          }
         }
         // move the stabiliser only when it must: first finite maximum, or growth beyond 2^8
         float corr = 1.f;
@@ -339,10 +368,18 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         }
         const float m_sub = m_use == -INFINITY ? 0.f : m_use;
         float rs = 0.f;
+        if (fast) {
 #pragma unroll
-        for (int c = 0; c < kUmKeys; ++c) {
-          x[c] = fast_exp2(x[c] - m_sub);
-          rs += x[c];
+          for (int c = 0; c < kUmKeys; ++c) {
+            x[c] = fast_exp2(fmaf(x[c], sc, -m_sub));
+            rs += x[c];
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kUmKeys; ++c) {
+            x[c] = fast_exp2(x[c] - m_sub);
+            rs += x[c];
+          }
         }
         l_run = l_run * corr + rs;
         // the previous P V of this group must be done: O stable, P buffer free
