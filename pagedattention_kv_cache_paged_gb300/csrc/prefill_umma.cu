@@ -80,7 +80,9 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   uint64_t* p_full = bars + 15;   // [2] per group: P_k written, O_k rescaled
   uint64_t* pv_done = bars + 17;  // [2] per group: O_k += P_k V finished
   uint64_t* fin = bars + 19;
+  uint64_t* mready = bars + 20;   // [8] per tile slot: the sub-tile mask below is written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 512);
+  uint32_t* kmask = reinterpret_cast<uint32_t*>(base + 768);  // [8] sub-tiles holding data, per tile slot
   uint8_t* qs = base + 1024;                       // [2][Q tile]
   uint8_t* ks = qs + 2 * Cfg::kQBytes;             // [3 stages][K tile]
   uint8_t* vs = ks + kUmKStages * Cfg::kKvBytes;   // [2 stages][V tile]
@@ -111,6 +113,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
     }
     mbar_init(q_ready, 256);
     mbar_init(fin, 1);
+    for (int s = 0; s < 8; ++s) mbar_init(&mready[s], 1);
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -185,6 +188,16 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                 bytes += kHalves * 2048;
               }
             }
+          }
+          if (!is_v) {
+            // publish which sub-tiles hold data; the softmax groups read it instead of the table.
+            // Slot i % 8 was last read for tile i - 8, which both groups finished long ago: this
+            // lane cannot run more than 4 tiles ahead of them (K ring depth + one S in flight).
+            unsigned m = 0;
+#pragma unroll
+            for (int sub = 0; sub < kUmSub; ++sub) m |= (ys[sub] >= 0 ? 1u : 0u) << sub;
+            kmask[i & 7] = m;
+            mbar_arrive(&mready[i & 7]);
           }
           uint8_t* st = ring + s * Cfg::kKvBytes;
           if (bytes == 0) {
@@ -314,20 +327,15 @@ __global__ void __launch_bounds__(kUmThreads, 1)
     for (int64_t t = T0; t < T1 && alive;) {
       const Seg sg = segment_at(t);
       if (!sg.ok && threadIdx.x == 0) raise_error(a.err, PA_DEVERR_QUERY_LOC);
-      const int32_t* table = a.block_table + (int64_t)sg.b * a.bt_stride;
       const int64_t bound = (sg.ok && tok >= t && tok < sg.seg1) ? sg.pos0 + (tok - sg.q0) : -1;
       const int nt = tiles_of(sg);
       for (int tile = 0; tile < nt; ++tile, ++i) {
         const int64_t kb = (int64_t)tile * kUmKeys;
-        unsigned loaded = 0;
-#pragma unroll
-        for (int sub = 0; sub < kUmSub; ++sub) {
-          const int64_t k0 = kb + sub * 16;
-          if (k0 < sg.kv_end) {
-            const int blk = __ldg(table + (k0 >> a.block_shift));
-            if (blk >= 0 && blk < a.num_blocks) loaded |= 1u << sub;
-          }
+        if (!__all_sync(0xffffffffu, mbar_wait(&mready[i & 7], (unsigned)((i >> 3) & 1), a.err))) {
+          alive = false;
+          break;
         }
+        const unsigned loaded = kmask[i & 7];
         if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], (unsigned)(i & 1), a.err))) {
           alive = false;
           break;
@@ -353,10 +361,17 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           for (int c = 0; c < kUmKeys; ++c) mx = fmaxf(mx, x[c]);
           mx *= sc;
         } else {
+          // bit c of `keep`: key kb + c is loaded and inside the causal bound
+          uint64_t keep = 0;
+#pragma unroll
+          for (int sub = 0; sub < kUmSub; ++sub)
+            if ((loaded >> sub) & 1u) keep |= 0xFFFFull << (16 * sub);
+          const int64_t lim = bound - kb;  // keys c <= lim are causal
+          if (lim < 0) keep = 0;
+          else if (lim < kUmKeys - 1) keep &= (2ull << lim) - 1ull;
 #pragma unroll
           for (int c = 0; c < kUmKeys; ++c) {
-            const bool keep = ((loaded >> (c >> 4)) & 1u) && (kb + c <= bound);
-            x[c] = keep ? x[c] * sc : -INFINITY;
+            x[c] = ((keep >> c) & 1ull) ? x[c] * sc : -INFINITY;
             mx = fmaxf(mx, x[c]);
           }
         }
