@@ -38,8 +38,8 @@ constexpr int kUmRows = 2 * kUmTileRows;    // rows per CTA
 constexpr int kUmKeys = 64;                 // keys per K/V tile (N of S, K of PV)
 constexpr int kUmSub = kUmKeys / 16;
 constexpr int kUmTmemCols = 512;
-constexpr int kUmKStages = 3;               // K ring depth (S of the next tile is issued early)
-constexpr int kUmVStages = 2;               // V ring depth
+constexpr int kUmKStages = 4;               // K ring depth (S of the next tile is issued early)
+constexpr int kUmVStages = 4;               // V ring depth
 constexpr float kUmRescaleThreshold = 8.f;  // log2 units: O is rescaled when the max grows by > 2^8
 
 template <int D>
@@ -70,17 +70,17 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base);
-  uint64_t* kfull = bars + 0;     // [3]
-  uint64_t* kempty = bars + 3;    // [3]
-  uint64_t* vfull = bars + 6;     // [2]
-  uint64_t* vempty = bars + 8;    // [2]
-  uint64_t* q_ready = bars + 10;
-  uint64_t* s_full = bars + 11;   // [2] per group: S_k computed
-  uint64_t* s_free = bars + 13;   // [2] per group: S_k read out of TMEM
-  uint64_t* p_full = bars + 15;   // [2] per group: P_k written, O_k rescaled
-  uint64_t* pv_done = bars + 17;  // [2] per group: O_k += P_k V finished
-  uint64_t* fin = bars + 19;
-  uint64_t* mready = bars + 20;   // [8] per tile slot: the sub-tile mask below is written
+  uint64_t* kfull = bars + 0;     // [4]
+  uint64_t* kempty = bars + 4;    // [4] completes when both groups' S products have read the tile
+  uint64_t* vfull = bars + 8;     // [4]
+  uint64_t* vempty = bars + 12;   // [4] completes when both groups' P V products have read the tile
+  uint64_t* q_ready = bars + 16;
+  uint64_t* s_full = bars + 17;   // [2] per group: S_k computed
+  uint64_t* s_free = bars + 19;   // [2] per group: S_k read out of TMEM
+  uint64_t* p_full = bars + 21;   // [2] per group: P_k written, O_k rescaled
+  uint64_t* pv_done = bars + 23;  // [2] per group: O_k += P_k V finished
+  uint64_t* fin = bars + 25;
+  uint64_t* mready = bars + 26;   // [8] per tile slot: the sub-tile mask below is written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 512);
   uint32_t* kmask = reinterpret_cast<uint32_t*>(base + 768);  // [8] sub-tiles holding data, per tile slot
   uint8_t* qs = base + 1024;                       // [2][Q tile]
@@ -101,11 +101,13 @@ __global__ void __launch_bounds__(kUmThreads, 1)
     prefetch_tensormap(&vmap);
     for (int s = 0; s < kUmKStages; ++s) {
       mbar_init(&kfull[s], 1);
-      mbar_init(&kempty[s], 1);
+      mbar_init(&kempty[s], 2);
+    }
+    for (int s = 0; s < kUmVStages; ++s) {
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 2);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&vfull[s], 1);
-      mbar_init(&vempty[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&s_free[s], 128);
       mbar_init(&p_full[s], 128);
@@ -241,58 +243,48 @@ __global__ void __launch_bounds__(kUmThreads, 1)
       };
       auto issue_pv = [&](int k, int i) {
         const uint32_t pa_ = smem_u32(ps + k * Cfg::kPBytes);
-        const uint32_t va = smem_u32(vs + (i & 1) * Cfg::kKvBytes);
+        const uint32_t va = smem_u32(vs + (i % kUmVStages) * Cfg::kKvBytes);
 #pragma unroll
         for (int kk = 0; kk < kUmKeys / 16; ++kk)
           umma_ss(tO(k), umma_desc_sw128(pa_ + kk * 32, 16, 1024),
                   umma_desc_sw128(va + kk * 2048, Cfg::kKvHalf, 1024), id_pv, (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&pv_done[k]);
       };
-      auto kwait = [&](int j) {
-        return mbar_wait(&kfull[j % kUmKStages], (unsigned)((j / kUmKStages) & 1), a.err);
-      };
+      // Event-driven issue: each group's next S (needs its previous S read out and the K tile) and
+      // next P V (needs its P and the V tile) are issued as soon as they are ready, so a slow group
+      // never holds back the other group's products.
       bool alive = mbar_wait(q_ready, 0, a.err);
-      if (alive && n_all > 0) {
-        alive = kwait(0);
-        if (alive) {
-          tc_fence_after();
-          issue_s(0, 0);
-          issue_s(1, 0);
-          umma_commit(&kempty[0]);
-        }
-      }
-      for (int i = 0; i < n_all && alive; ++i) {
-        // next tile's S products as soon as each group has read its S out of TMEM
-        if (i + 1 < n_all) {
-          if (!kwait(i + 1) || !mbar_wait(&s_free[0], (unsigned)(i & 1), a.err)) {
-            alive = false;
-            break;
+      int next_s[2] = {0, 0}, next_pv[2] = {0, 0};
+      int idle = 0;
+      while (alive && (next_pv[0] < n_all || next_pv[1] < n_all)) {
+        bool progress = false;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int j = next_s[k];
+          if (j < n_all && (j == 0 || mbar_test(&s_free[k], (unsigned)((j - 1) & 1))) &&
+              mbar_test(&kfull[j % kUmKStages], (unsigned)((j / kUmKStages) & 1))) {
+            tc_fence_after();
+            issue_s(k, j);
+            umma_commit(&kempty[j % kUmKStages]);
+            next_s[k] = j + 1;
+            progress = true;
           }
-          tc_fence_after();
-          issue_s(0, i + 1);
-          if (!mbar_wait(&s_free[1], (unsigned)(i & 1), a.err)) {
-            alive = false;
-            break;
+          const int jp = next_pv[k];
+          if (jp < next_s[k] && mbar_test(&p_full[k], (unsigned)(jp & 1)) &&
+              mbar_test(&vfull[jp % kUmVStages], (unsigned)((jp / kUmVStages) & 1))) {
+            tc_fence_after();
+            issue_pv(k, jp);
+            umma_commit(&vempty[jp % kUmVStages]);
+            next_pv[k] = jp + 1;
+            progress = true;
           }
-          tc_fence_after();
-          issue_s(1, i + 1);
-          umma_commit(&kempty[(i + 1) % kUmKStages]);
         }
-        // this tile's P V products
-        if (!mbar_wait(&vfull[i & 1], (unsigned)((i >> 1) & 1), a.err) ||
-            !mbar_wait(&p_full[0], (unsigned)(i & 1), a.err)) {
+        if (progress) {
+          idle = 0;
+        } else if (++idle > kWaitSpins ||
+                   (idle > 4096 && (*reinterpret_cast<const volatile unsigned*>(a.err) & PA_DEVERR_TIMEOUT))) {
           alive = false;
-          break;
         }
-        tc_fence_after();
-        issue_pv(0, i);
-        if (!mbar_wait(&p_full[1], (unsigned)(i & 1), a.err)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(1, i);
-        umma_commit(&vempty[i & 1]);
       }
       if (!alive) raise_error(a.err, PA_DEVERR_TIMEOUT);
       if (n_all > 0) {
@@ -420,11 +412,11 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         // group 0 zeroes V rows that hold no data or lie past the context (group 1's P V is issued
         // after group 0's, so it sees the zeros too)
         if (grp == 0 && (kb + kUmKeys > sg.n || loaded != (1u << kUmSub) - 1u)) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&vfull[i & 1], (unsigned)((i >> 1) & 1), a.err))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&vfull[i % kUmVStages], (unsigned)((i / kUmVStages) & 1), a.err))) {
             alive = false;
             break;
           }
-          uint8_t* vst = vs + (i & 1) * Cfg::kKvBytes;
+          uint8_t* vst = vs + (i % kUmVStages) * Cfg::kKvBytes;
           for (int e = r; e < kUmKeys * 8 * kHalves; e += 128) {
             const int key = e / (8 * kHalves);
             const int c = e % (8 * kHalves);
