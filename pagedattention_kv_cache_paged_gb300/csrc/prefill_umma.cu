@@ -270,7 +270,9 @@ __global__ void __launch_bounds__(kUmThreads, 1)
             progress = true;
           }
           const int jp = next_pv[k];
-          if (jp < next_s[k] && mbar_test(&p_full[k], (unsigned)(jp & 1)) &&
+          // group 1's P V follows group 0's for the same tile: group 0 zeroes the tile's stale V
+          // rows before it signals p_full, and group 1 must not read them earlier
+          if (jp < next_s[k] && (k == 0 || next_pv[0] > jp) && mbar_test(&p_full[k], (unsigned)(jp & 1)) &&
               mbar_test(&vfull[jp % kUmVStages], (unsigned)((jp / kUmVStages) & 1))) {
             tc_fence_after();
             issue_pv(k, jp);
