@@ -38,8 +38,8 @@ constexpr int kUmRows = 2 * kUmTileRows;    // rows per CTA
 constexpr int kUmKeys = 64;                 // keys per K/V tile (N of S, K of PV)
 constexpr int kUmSub = kUmKeys / 16;
 constexpr int kUmTmemCols = 512;
-constexpr int kUmKStages = 4;               // K ring depth (S of the next tile is issued early)
-constexpr int kUmVStages = 4;               // V ring depth
+constexpr int kUmKStages = 3;               // K ring depth
+constexpr int kUmVStages = 3;               // V ring depth
 constexpr float kUmRescaleThreshold = 8.f;  // log2 units: O is rescaled when the max grows by > 2^8
 
 template <int D>
@@ -50,7 +50,7 @@ struct UmCfg {
   static constexpr int kKvHalf = kUmKeys * 128;      // one 64-column half of a K or V tile
   static constexpr int kKvBytes = kUmKeys * D * 2;
   static constexpr int kPBytes = kUmTileRows * kUmKeys * 2;
-  static constexpr int kSmemBytes = 1024 + 1024 + 2 * kQBytes + (kUmKStages + kUmVStages) * kKvBytes + 2 * kPBytes;
+  static constexpr int kSmemBytes = 1024 + 1024 + 2 * kQBytes + (kUmKStages + kUmVStages) * kKvBytes + 4 * kPBytes;
 };
 
 // Byte offset of (row r, 8-element chunk c) in a [half][rows][128 B] swizzled operand.
@@ -70,23 +70,24 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base);
-  uint64_t* kfull = bars + 0;     // [4]
-  uint64_t* kempty = bars + 4;    // [4] completes when both groups' S products have read the tile
-  uint64_t* vfull = bars + 8;     // [4]
-  uint64_t* vempty = bars + 12;   // [4] completes when both groups' P V products have read the tile
-  uint64_t* q_ready = bars + 16;
-  uint64_t* s_full = bars + 17;   // [2] per group: S_k computed
-  uint64_t* s_free = bars + 19;   // [2] per group: S_k read out of TMEM
-  uint64_t* p_full = bars + 21;   // [2] per group: P_k written, O_k rescaled
-  uint64_t* pv_done = bars + 23;  // [2] per group: O_k += P_k V finished
-  uint64_t* fin = bars + 25;
-  uint64_t* mready = bars + 26;   // [8] per tile slot: the sub-tile mask below is written
+  uint64_t* kfull = bars + 0;     // [3]
+  uint64_t* kempty = bars + 3;    // [3] completes when both groups' S products have read the tile
+  uint64_t* vfull = bars + 6;     // [3]
+  uint64_t* vempty = bars + 9;    // [3] completes when both groups' P V products have read the tile
+  uint64_t* q_ready = bars + 12;
+  // per group k and buffer b (tile j uses buffer j % 2): [2 * k + b]
+  uint64_t* s_full = bars + 13;   // S_k^b computed
+  uint64_t* s_free = bars + 17;   // S_k^b read out of TMEM
+  uint64_t* p_full = bars + 21;   // P_k^b written (and O_k rescaled)
+  uint64_t* pv_done = bars + 25;  // O_k += P_k^b V finished
+  uint64_t* fin = bars + 29;
+  uint64_t* mready = bars + 30;   // [8] per tile slot: the sub-tile mask below is written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 512);
   uint32_t* kmask = reinterpret_cast<uint32_t*>(base + 768);  // [8] sub-tiles holding data, per tile slot
   uint8_t* qs = base + 1024;                       // [2][Q tile]
   uint8_t* ks = qs + 2 * Cfg::kQBytes;             // [3 stages][K tile]
   uint8_t* vs = ks + kUmKStages * Cfg::kKvBytes;   // [2 stages][V tile]
-  uint8_t* ps = vs + kUmVStages * Cfg::kKvBytes;   // [2 groups][P tile]
+  uint8_t* ps = vs + kUmVStages * Cfg::kKvBytes;   // [2 groups][2 buffers][P tile]
 
   const int kvh = blockIdx.x % a.n_kv_heads;
   const int64_t T0 = (int64_t)(blockIdx.x / a.n_kv_heads) * kQB;
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 2);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 4; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&s_free[s], 128);
       mbar_init(&p_full[s], 128);
@@ -124,9 +125,9 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // S_k at columns [64k, 64k + 64), O_k at [128 + 128k, 128 + 128k + D)
-  auto tS = [&](int k) { return tmem + 64u * (uint32_t)k; };
-  auto tO = [&](int k) { return tmem + 128u + 128u * (uint32_t)k; };
+  // S_k^b at columns [64 (2k + b), +64), O_k at [256 + 128k, +D)
+  auto tS = [&](int k, int b) { return tmem + 64u * (uint32_t)(2 * k + b); };
+  auto tO = [&](int k) { return tmem + 256u + 128u * (uint32_t)k; };
 
   struct Seg {
     int b;
@@ -236,19 +237,19 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t qo = (kk >> 2) * Cfg::kQHalf + (kk & 3) * 32;
           const uint32_t ko = (kk >> 2) * Cfg::kKvHalf + (kk & 3) * 32;
-          umma_ss(tS(k), umma_desc_sw128(qa + qo, 16, 1024), umma_desc_sw128(ka + ko, 16, 1024), id_s,
+          umma_ss(tS(k, i & 1), umma_desc_sw128(qa + qo, 16, 1024), umma_desc_sw128(ka + ko, 16, 1024), id_s,
                   kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[k]);
+        umma_commit(&s_full[2 * k + (i & 1)]);
       };
       auto issue_pv = [&](int k, int i) {
-        const uint32_t pa_ = smem_u32(ps + k * Cfg::kPBytes);
+        const uint32_t pa_ = smem_u32(ps + (2 * k + (i & 1)) * Cfg::kPBytes);
         const uint32_t va = smem_u32(vs + (i % kUmVStages) * Cfg::kKvBytes);
 #pragma unroll
         for (int kk = 0; kk < kUmKeys / 16; ++kk)
           umma_ss(tO(k), umma_desc_sw128(pa_ + kk * 32, 16, 1024),
                   umma_desc_sw128(va + kk * 2048, Cfg::kKvHalf, 1024), id_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&pv_done[k]);
+        umma_commit(&pv_done[2 * k + (i & 1)]);
       };
       // Event-driven issue: each group's next S (needs its previous S read out and the K tile) and
       // next P V (needs its P and the V tile) are issued as soon as they are ready, so a slow group
@@ -260,8 +261,9 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         bool progress = false;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
+          // S_k(j) overwrites buffer j % 2, last holding S_k(j - 2)
           const int j = next_s[k];
-          if (j < n_all && (j == 0 || mbar_test(&s_free[k], (unsigned)((j - 1) & 1))) &&
+          if (j < n_all && (j < 2 || mbar_test(&s_free[2 * k + (j & 1)], (unsigned)(((j >> 1) - 1) & 1))) &&
               mbar_test(&kfull[j % kUmKStages], (unsigned)((j / kUmKStages) & 1))) {
             tc_fence_after();
             issue_s(k, j);
@@ -272,7 +274,8 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           const int jp = next_pv[k];
           // group 1's P V follows group 0's for the same tile: group 0 zeroes the tile's stale V
           // rows before it signals p_full, and group 1 must not read them earlier
-          if (jp < next_s[k] && (k == 0 || next_pv[0] > jp) && mbar_test(&p_full[k], (unsigned)(jp & 1)) &&
+          if (jp < next_s[k] && (k == 0 || next_pv[0] > jp) &&
+              mbar_test(&p_full[2 * k + (jp & 1)], (unsigned)((jp >> 1) & 1)) &&
               mbar_test(&vfull[jp % kUmVStages], (unsigned)((jp / kUmVStages) & 1))) {
             tc_fence_after();
             issue_pv(k, jp);
@@ -302,7 +305,6 @@ __global__ void __launch_bounds__(kUmThreads, 1)
     const int64_t tok = T0 + row / G;
     const int head = kvh * G + row % G;
     uint8_t* q_tile = qs + grp * Cfg::kQBytes;
-    uint8_t* p_tile = ps + grp * Cfg::kPBytes;
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + (tok * a.n_q_heads + head) * D);
 #pragma unroll
@@ -330,7 +332,8 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           break;
         }
         const unsigned loaded = kmask[i & 7];
-        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], (unsigned)(i & 1), a.err))) {
+        const int bsel = i & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[2 * grp + bsel], (unsigned)((i >> 1) & 1), a.err))) {
           alive = false;
           break;
         }
@@ -339,13 +342,13 @@ __global__ void __launch_bounds__(kUmThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < kUmKeys; c0 += 32) {
           uint32_t v[32];
-          tmem_ld32(tS(grp) + lane_base + c0, v);
+          tmem_ld32(tS(grp, bsel) + lane_base + c0, v);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[c0 + j] = __uint_as_float(v[j]);
         }
         tc_fence_before();
-        mbar_arrive(&s_free[grp]);  // S_k may now be overwritten by the next tile's product
+        mbar_arrive(&s_free[2 * grp + bsel]);  // this S buffer may now take tile i + 2
         // a tile wholly inside this row's causal bound with every sub-tile loaded needs no mask
         const float sc = a.scale_log2;
         const bool fast = sc > 0.f && loaded == (1u << kUmSub) - 1u && kb + kUmKeys - 1 <= bound;
@@ -391,25 +394,28 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           }
         }
         l_run = l_run * corr + rs;
-        // the previous P V of this group must be done: O stable, P buffer free
-        if (i > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[grp], (unsigned)((i - 1) & 1), a.err))) {
+        // the P buffer of tile i - 2 must have been consumed, and O must be stable before a rescale
+        if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[2 * grp + bsel], (unsigned)(((i >> 1) - 1) & 1), a.err))) {
+          alive = false;
+          break;
+        }
+        if (i > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+          const int pb = (i - 1) & 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[2 * grp + pb], (unsigned)(((i - 1) >> 1) & 1), a.err))) {
             alive = false;
             break;
           }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t v[32];
-              tmem_ld32(tO(grp) + lane_base + c0, v);
-              tmem_wait_ld();
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tO(grp) + lane_base + c0, v);
+            tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * corr);
-              tmem_st32(tO(grp) + lane_base + c0, v);
-            }
-            tmem_wait_st();
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * corr);
+            tmem_st32(tO(grp) + lane_base + c0, v);
           }
+          tmem_wait_st();
         }
         // group 0 zeroes V rows that hold no data or lie past the context (group 1's P V is issued
         // after group 0's, so it sees the zeros too)
@@ -434,17 +440,17 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           w.y = pack2<kBf16>(x[8 * c + 2], x[8 * c + 3]);
           w.z = pack2<kBf16>(x[8 * c + 4], x[8 * c + 5]);
           w.w = pack2<kBf16>(x[8 * c + 6], x[8 * c + 7]);
-          *reinterpret_cast<uint4*>(p_tile + sw_off(r, c, kUmTileRows * 128)) = w;
+          *reinterpret_cast<uint4*>(ps + (2 * grp + bsel) * Cfg::kPBytes + sw_off(r, c, kUmTileRows * 128)) = w;
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&p_full[grp]);
+        mbar_arrive(&p_full[2 * grp + bsel]);
       }
       t = sg.seg1;
     }
     if (!alive && lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
     if (alive && i > 0) {
-      alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[grp], (unsigned)((i - 1) & 1), a.err));
+      alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[2 * grp + ((i - 1) & 1)], (unsigned)(((i - 1) >> 1) & 1), a.err));
       tc_fence_after();
     }
     const bool have = alive && i > 0 && l_run != 0.f;
