@@ -306,6 +306,8 @@ def main():
     ap.add_argument("--partition-tokens", type=int, default=0, help="split-K partition length (0 = library default)")
     ap.add_argument("--decode-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
+    ap.add_argument("--unfused", action="store_true",
+                    help="time paged_kv_write + paged_attention_decode as two calls instead of the fused call")
     ap.add_argument("--prefill-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05, 3 mma.sync")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -360,9 +362,29 @@ def main():
         if st:
             raise RuntimeError(f"paged_attention_decode status {st}")
 
+    def fused(layer):
+        kp, vp = pools[layer]
+        st = lib.paged_attention_decode_fused(ptr["out"], ptr["q"], ptr["kn"], ptr["vn"], ptr["slot"], kp.data_ptr(),
+                                              vp.data_ptr(), ptr["table"], bt_stride, ptr["ctx"], B, W.LLAMA_POOL, S,
+                                              scale, HQ, HKV, D, pa.PA_BF16, ptr["ws"], ws_bytes, sp)
+        if st:
+            raise RuntimeError(f"paged_attention_decode_fused status {st}")
+
+    use_fused = not args.unfused
+
+    def step_pre(layer):
+        if not use_fused:
+            write(layer)
+
+    def step_main(layer):
+        if use_fused:
+            fused(layer)
+        else:
+            decode(layer)
+
     for i in range(args.warmup):
-        write(i % args.layers)
-        decode(i % args.layers)
+        step_pre(i % args.layers)
+        step_main(i % args.layers)
     K = args.steps
     ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -373,9 +395,9 @@ def main():
     ev0.record(stream)
     for i in range(K):
         layer = i % args.layers
-        write(layer)
+        step_pre(layer)
         ev_dec[i][0].record(stream)
-        decode(layer)
+        step_main(layer)
         ev_dec[i][1].record(stream)
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -389,7 +411,7 @@ def main():
     ms_per_step = total_ms / K
     value = step_bytes * K * world / (total_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    achieved = kvb / (dec_ms * 1e-3) / 1e9
+    achieved = (step_bytes if use_fused else kvb) / (dec_ms * 1e-3) / 1e9
     if pa.device_error_flags() != 0:
         raise RuntimeError("device error word set during the benchmark")
 
@@ -406,8 +428,8 @@ def main():
         def e2e_step(i):
             for k in host:
                 devs[k].copy_(host[k], non_blocking=True)
-            write(i % args.layers)
-            decode(i % args.layers)
+            step_pre(i % args.layers)
+            step_main(i % args.layers)
             host_out.copy_(out, non_blocking=True)
 
         for i in range(3):
@@ -432,7 +454,8 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V, bf16)",
-        "config": {"workload": "llama3_8b_serving_decode: paged_kv_write of 64 tokens + paged decode attention, "
+        "config": {"workload": "llama3_8b_serving_decode: write of the 64 new tokens through slot_mapping + paged "
+                               "decode attention (" + ("one fused call" if use_fused else "two calls") + "), "
                                "32q/8kv heads, head_dim 128, block_size 16, batch 64, context U[512,4096], "
                                "40,000-block shuffled pool",
                    "context_tokens": sum(lens), "batch": B,
@@ -445,7 +468,9 @@ def main():
         "pct_hbm_spec_8000": value / 8000.0,
         "decode_tok_s_attention_only": B * world / (LLAMA_LAYERS * ms_per_step * 1e-3),
         "kernel_us": {"decode_call": dec_ms * 1e3, "step": ms_per_step * 1e3},
-        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (partition + merge kernels)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("paged_attention_decode_fused (write + partition kernel, then merge kernel)" if use_fused
+                                else "paged_attention_decode (partition + merge kernels)"),
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None},
         "gpu_launches": launches,

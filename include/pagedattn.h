@@ -126,6 +126,27 @@ PA_API int paged_attention_decode(void* out, const void* q, const void* k_pool, 
                            float scale, int n_q_heads, int n_kv_heads, int head_dim, pa_dtype dtype,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * paged_attention_decode_fused — paged_kv_write of each sequence's new token followed by
+ * paged_attention_decode, in one launch (nanoserve Day 19, "What I added today": the fused paged
+ * read writes this step's K/V into the block pool and then attends over the whole history through
+ * the block table, without rebuilding it).
+ *   k_new, v_new   [batch][n_kv_heads][head_dim], dtype: the new token of sequence b is row b
+ *   slot_mapping   int64 [batch]: slot of that token, which must be the slot of position
+ *                  context_lens[b] - 1 (the decode convention) or negative (no write).  Any other
+ *                  slot is neither written nor used: the device records PA_DEVERR_SLOT, checked
+ *                  mode returns PA_ERANGE.
+ *   k_pool, v_pool written in place (the new rows), then read.
+ * Every other argument, the output and the workspace rules are those of paged_attention_decode; the
+ * result (output and pools) is bit-identical to the two separate calls.
+ */
+PA_API int paged_attention_decode_fused(void* out, const void* q, const void* k_new, const void* v_new,
+                                        const int64_t* slot_mapping, void* k_pool, void* v_pool,
+                                        const int32_t* block_table, int64_t block_table_stride,
+                                        const int32_t* context_lens, int batch, int64_t num_blocks, int block_size,
+                                        float scale, int n_q_heads, int n_kv_heads, int head_dim, pa_dtype dtype,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* Workspace bytes paged_attention_decode needs for split-K with these sizes (0 if it never splits). */
 PA_API size_t paged_attention_decode_workspace_size(int batch, int64_t block_table_stride, int block_size,
                                              int n_q_heads, int n_kv_heads, int head_dim);

@@ -33,6 +33,8 @@ SIGNATURES = {
     "paged_attention_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _i64, _i32, _f32, _i32, _i32,
                                       _i32, _i32, _vp, _sz, _vp]),
     "paged_attention_decode_workspace_size": (_sz, [_i32, _i64, _i32, _i32, _i32, _i32]),
+    "paged_attention_decode_fused": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _i64, _i32,
+                                            _f32, _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
     "paged_attention_prefill": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i32, _i64, _i32, _f32,
                                        _i32, _i32, _i32, _i32, _vp]),
     "copy_blocks": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp]),
@@ -190,6 +192,40 @@ def paged_attention_decode(q, k_pool, v_pool, block_table, context_lens, scale=N
                                     _dev(context_lens, "context_lens", torch.int32), B, NB, S, float(scale),
                                     Hq, Hkv, D, _code(dt), ws_ptr, ws_bytes, _stream(stream))
     _check("paged_attention_decode", st)
+    return out
+
+
+def paged_attention_decode_fused(q, k_new, v_new, slot_mapping, k_pool, v_pool, block_table, context_lens,
+                                 scale=None, out=None, workspace="auto", stream=None):
+    """Write each sequence's new token (row b of ``k_new, v_new [B, Hkv, D]``) to
+    ``slot_mapping[b]`` — the slot of its last context position — and attend, in one launch.
+    Same result as :func:`paged_kv_write` followed by :func:`paged_attention_decode`."""
+    lib = load_library()
+    NB, S, Hkv, D = _pool_dims(k_pool, v_pool)
+    if q.dim() != 3 or q.shape[2] != D:
+        raise ValueError("q must be [batch, n_q_heads, head_dim]")
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or slot_mapping.numel() != B:
+        raise ValueError("k_new / v_new must be [batch, n_kv_heads, head_dim] and slot_mapping [batch]")
+    if block_table.dim() != 2 or block_table.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_table must be [batch, max_blocks] and context_lens [batch]")
+    if block_table.stride(1) != 1:
+        raise ValueError("block_table rows must be contiguous")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dt = k_pool.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    bt_stride = int(block_table.stride(0))
+    ws = _workspace(q.device, decode_workspace_size(B, bt_stride, S, Hq, Hkv, D)) if workspace == "auto" else workspace
+    st = lib.paged_attention_decode_fused(
+        _dev(out, "out", dt), _dev(q, "q", dt), _dev(k_new, "k_new", dt), _dev(v_new, "v_new", dt),
+        _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_pool, "k_pool", dt), _dev(v_pool, "v_pool", dt),
+        _dev(block_table, "block_table", torch.int32, contiguous=False), bt_stride,
+        _dev(context_lens, "context_lens", torch.int32), B, NB, S, float(scale), Hq, Hkv, D, _code(dt),
+        _dev(ws, "workspace", torch.uint8) if ws is not None else None, int(ws.numel()) if ws is not None else 0,
+        _stream(stream))
+    _check("paged_attention_decode_fused", st)
     return out
 
 

@@ -241,11 +241,11 @@ size_t paged_attention_decode_workspace_size(int batch, int64_t block_table_stri
   return workspace_layout((int64_t)batch * n_q_heads, max_parts, head_dim).bytes;
 }
 
-int paged_attention_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
-                           const int32_t* block_table, int64_t block_table_stride,
-                           const int32_t* context_lens, int batch, int64_t num_blocks, int block_size,
-                           float scale, int n_q_heads, int n_kv_heads, int head_dim, pa_dtype dtype,
-                           void* workspace, size_t workspace_bytes, void* stream) {
+static int decode_impl(void* out, const void* q, const void* k_pool, const void* v_pool,
+                       const int32_t* block_table, int64_t block_table_stride, const int32_t* context_lens,
+                       int batch, int64_t num_blocks, int block_size, float scale, int n_q_heads, int n_kv_heads,
+                       int head_dim, pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream,
+                       const void* k_new, const void* v_new, const int64_t* slot_mapping) {
   int rc = check_dtype(dtype);
   if (rc) return rc;
   rc = check_heads(n_q_heads, n_kv_heads, head_dim);
@@ -255,14 +255,33 @@ int paged_attention_decode(void* out, const void* q, const void* k_pool, const v
   if (batch == 0) return PA_OK;
   if (!out || !q || !k_pool || !v_pool || !block_table || !context_lens) return PA_EINVAL;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PA_EINVAL;
+  const bool fused = k_new != nullptr || v_new != nullptr || slot_mapping != nullptr;
+  if (fused && (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new))) return PA_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned* err = nullptr;
   int sms = 0;
   rc = device_info(&err, &sms);
   if (rc) return rc;
   if (checked()) {
-    rc = validate_tables(block_table, block_table_stride, context_lens, batch, num_blocks, block_size, s, nullptr);
+    std::vector<int32_t> lens;
+    rc = validate_tables(block_table, block_table_stride, context_lens, batch, num_blocks, block_size, s, &lens);
     if (rc) return rc;
+    if (fused) {
+      std::vector<int64_t> slots;
+      std::vector<int32_t> table;
+      rc = copy_to_host(slots, slot_mapping, batch, s);
+      if (rc) return rc;
+      rc = copy_to_host(table, block_table, (int64_t)batch * block_table_stride, s);
+      if (rc) return rc;
+      for (int b = 0; b < batch; ++b) {
+        if (slots[(size_t)b] < 0) continue;
+        const int64_t last = (int64_t)lens[(size_t)b] - 1;
+        if (last < 0) return PA_ERANGE;
+        const int64_t expect = (int64_t)table[(size_t)(b * block_table_stride + last / block_size)] * block_size +
+                               last % block_size;
+        if (slots[(size_t)b] != expect) return PA_ERANGE;
+      }
+    }
   }
   const int64_t kernel_opt = g_options[PA_OPT_DECODE_KERNEL].load();
   const bool tc_ok = decode_tc_supported(dtype, block_size, head_dim, n_q_heads / n_kv_heads, num_blocks);
@@ -308,6 +327,13 @@ int paged_attention_decode(void* out, const void* q, const void* k_pool, const v
     a.ws_l = reinterpret_cast<float*>(base + ws.off_l);
   }
   a.err = err;
+  if (fused) {
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.slot_mapping = slot_mapping;
+    a.k_pool_w = const_cast<void*>(k_pool);
+    a.v_pool_w = const_cast<void*>(v_pool);
+  }
   int launches = 0;
   cudaError_t e = use_tc ? launch_decode_tc(a, dtype, s, &launches) : launch_attn_simt(a, dtype, s, &launches);
   if (e == cudaSuccess && max_parts > 1) {
@@ -326,6 +352,28 @@ int paged_attention_decode(void* out, const void* q, const void* k_pool, const v
     e = launch_lse_merge(m, dtype, s, &launches);
   }
   return finish(e, launches);
+}
+
+int paged_attention_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_table, int64_t block_table_stride,
+                           const int32_t* context_lens, int batch, int64_t num_blocks, int block_size,
+                           float scale, int n_q_heads, int n_kv_heads, int head_dim, pa_dtype dtype,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(out, q, k_pool, v_pool, block_table, block_table_stride, context_lens, batch, num_blocks,
+                     block_size, scale, n_q_heads, n_kv_heads, head_dim, dtype, workspace, workspace_bytes, stream,
+                     nullptr, nullptr, nullptr);
+}
+
+int paged_attention_decode_fused(void* out, const void* q, const void* k_new, const void* v_new,
+                                 const int64_t* slot_mapping, void* k_pool, void* v_pool,
+                                 const int32_t* block_table, int64_t block_table_stride,
+                                 const int32_t* context_lens, int batch, int64_t num_blocks, int block_size,
+                                 float scale, int n_q_heads, int n_kv_heads, int head_dim, pa_dtype dtype,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch > 0 && (!k_new || !v_new || !slot_mapping)) return PA_EINVAL;
+  return decode_impl(out, q, k_pool, v_pool, block_table, block_table_stride, context_lens, batch, num_blocks,
+                     block_size, scale, n_q_heads, n_kv_heads, head_dim, dtype, workspace, workspace_bytes, stream,
+                     k_new, v_new, slot_mapping);
 }
 
 int paged_attention_prefill(void* out, const void* q, const int32_t* query_start_loc, int64_t total_q,

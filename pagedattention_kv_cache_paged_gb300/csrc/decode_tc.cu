@@ -104,6 +104,22 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
 
   const int32_t* table = a.block_table + (int64_t)b * a.bt_stride;
   const int bmask = a.block_size - 1;
+  // fused write: the CTA holding the last context position writes this step's K/V row of its KV
+  // head there and uses it straight from k_new / v_new (nanoserve Day 19, "What I added today":
+  // write this step's K/V, then attend over the whole history)
+  int64_t new_row = -1;
+  if (a.k_new != nullptr && len > 0 && part == n_parts_row - 1) {
+    const int64_t last = len - 1;
+    const int64_t s_new = __ldg(a.slot_mapping + b);
+    const int blk_last = __ldg(table + (last >> a.block_shift));
+    const int64_t expect = (blk_last >= 0 && blk_last < a.num_blocks)
+                               ? ((int64_t)blk_last << a.block_shift) + (last & bmask) : -2;
+    if (s_new >= 0) {
+      if (s_new == expect) new_row = s_new;
+      else if (threadIdx.x == 0) raise_error(a.err, PA_DEVERR_SLOT);
+    }
+  }
+  const int patch_tile = new_row >= 0 ? (int)((len - 1 - t_begin) / kTile) : -1;
   uint64_t* my_bars = bars + warp * kStages;
   uint8_t* my_stages = stages + warp * kStages * kStageBytes;
 
@@ -177,6 +193,23 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
     const uint32_t k_base = smem_u32(st);
     const uint32_t v_base = smem_u32(st + kHalves * kHalfBytes);
     if (blk >= 0 && blk < a.num_blocks) {
+      if (warp + kTcWarps * j == patch_tile) {
+        // this step's token: row (len - 1) mod 16 of the tile, from k_new / v_new, into shared
+        // memory (swizzled like the TMA boxes) and into the pool
+        constexpr int kChunks = D / 8;
+        const int r = (int)((len - 1) & (kTile - 1));
+        if (lane < 2 * kChunks) {
+          const bool isv = lane >= kChunks;
+          const int c = lane % kChunks;
+          const int64_t src_off = ((int64_t)b * a.n_kv_heads + kvh) * D + c * 8;
+          const uint4 val = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(isv ? a.v_new : a.k_new) + src_off));
+          *reinterpret_cast<uint4*>(st + ((isv ? kHalves : 0) + (c >> 3)) * kHalfBytes + r * 128 +
+                                    (((c & 7) ^ (r & 7)) << 4)) = val;
+          T* dst = static_cast<T*>(isv ? a.v_pool_w : a.k_pool_w) + (new_row * a.n_kv_heads + kvh) * D + c * 8;
+          *reinterpret_cast<uint4*>(dst) = val;
+        }
+        __syncwarp();
+      }
       if (valid < kTile) {
         // zero the V rows past the end (both halves): 16-byte stores, rows valid..15
         const int nz = (kTile - valid) * 8 * kHalves;

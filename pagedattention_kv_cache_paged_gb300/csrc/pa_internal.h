@@ -61,6 +61,14 @@ struct AttnArgs {
   float* ws_l;                     // [rows * n_q_heads][max_parts]
   float* ws_acc;                   // [rows * n_q_heads][max_parts][head_dim]
   unsigned* err;
+  // fused K/V write (decode only; all nullptr otherwise): sequence b's new token k_new[b], v_new[b]
+  // ([batch][n_kv_heads][head_dim]) goes to pool row slot_mapping[b], which must be the slot of its
+  // last context position; the CTA reading that position takes the row from k_new/v_new directly.
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+  void* k_pool_w;                  // the pools again, writable
+  void* v_pool_w;
 };
 
 struct MergeArgs {
