@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(const AttnAr
   const int dsub = lane % kLanesPerRow;
   const int rsub = lane / kLanesPerRow;
 
+  pdl_launch_dependents();  // the split-K merge may begin launching; it waits for this grid's results
+
   // ---- which sequence and how many keys this row sees --------------------------------------
   const int64_t max_len = a.bt_stride << a.block_shift;
   int b;

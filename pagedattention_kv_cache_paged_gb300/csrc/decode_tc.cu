@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   auto tile_t0 = [&](int j) -> int64_t { return t_begin + (int64_t)(warp + kTcWarps * j) * kTile; };
   auto tile_block = [&](int j) -> int { return __ldg(table + (tile_t0(j) >> a.block_shift)); };
 
+  pdl_launch_dependents();  // the split-K merge may begin launching; it waits for this grid's results
   if (lane == 0) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);

@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
   constexpr int kPer = D / 32;
   const int64_t row = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_wait_primary();  // partials of the partition kernel are complete and visible
   if (row >= a.rows) return;
   int parts = a.n_parts;
   if (a.context_lens != nullptr) {
@@ -58,16 +59,34 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
   for (int i = 0; i < kPer; ++i) o[i] = Elt<T>::from_float(acc[i] * inv);
 }
 
+// Launched with programmatic stream serialization when it follows a partition kernel in the same
+// call: its CTAs may be scheduled while the partition grid drains and then wait (griddepcontrol) for
+// that grid's completion, which hides the launch gap between the two kernels.
+template <typename T, int D>
+static cudaError_t launch_merge_d(const MergeArgs& a, cudaStream_t s, unsigned blocks, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<T, D>, a);
+}
+
 template <typename T>
 static cudaError_t launch_merge_t(const MergeArgs& a, cudaStream_t s) {
   const int64_t blocks = (a.rows + kMergeWarps - 1) / kMergeWarps;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const bool pdl = a.context_lens != nullptr;  // internal merge right after the partition kernel
   switch (a.head_dim) {
-    case 64: lse_merge_kernel<T, 64><<<(unsigned)blocks, kMergeWarps * 32, 0, s>>>(a); break;
-    case 128: lse_merge_kernel<T, 128><<<(unsigned)blocks, kMergeWarps * 32, 0, s>>>(a); break;
+    case 64: return launch_merge_d<T, 64>(a, s, (unsigned)blocks, pdl);
+    case 128: return launch_merge_d<T, 128>(a, s, (unsigned)blocks, pdl);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_lse_merge(const MergeArgs& a, pa_dtype dt, cudaStream_t s, int* launches) {

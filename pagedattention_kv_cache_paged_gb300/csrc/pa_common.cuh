@@ -78,6 +78,13 @@ struct Elt<float> {
   __device__ __forceinline__ static float from_float(float x) { return x; }
 };
 
+// Programmatic dependent launch: let the next kernel in the stream start its launch now (its CTAs
+// still wait for this grid's completion before reading what it wrote).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the preceding grid in the stream has completed and its writes are visible (a no-op when
+// the kernel was launched without programmatic serialization).
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Resolve which sequence a prefill query row belongs to: the largest b with qsl[b] <= row.
 __device__ __forceinline__ int find_sequence(const int32_t* qsl, int batch, int64_t row) {
   int lo = 0, hi = batch - 1;
