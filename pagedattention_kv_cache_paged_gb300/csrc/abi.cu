@@ -291,7 +291,10 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
   int part_tokens = 0, max_parts = 1;
   plan_split(block_table_stride, block_size, &part_tokens, &max_parts);
   WsLayout ws = workspace_layout((int64_t)batch * n_q_heads, max_parts, head_dim);
-  if (max_parts > 1) {
+  // up to 8 partitions per row on the tensor-core path: one thread-block cluster per row merges
+  // through distributed shared memory, with neither workspace nor merge kernel
+  const bool cluster = use_tc && max_parts >= 2 && max_parts <= 8;
+  if (max_parts > 1 && !cluster) {
     if (workspace == nullptr) {
       max_parts = 1;
       part_tokens = (int)(block_table_stride * block_size);
@@ -320,12 +323,13 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
   a.head_dim = head_dim;
   a.part_tokens = part_tokens;
   a.max_parts = max_parts;
-  if (max_parts > 1) {
+  if (max_parts > 1 && !cluster) {
     char* base = static_cast<char*>(workspace);
     a.ws_acc = reinterpret_cast<float*>(base);
     a.ws_m = reinterpret_cast<float*>(base + ws.off_m);
     a.ws_l = reinterpret_cast<float*>(base + ws.off_l);
   }
+  a.cluster = cluster ? 1 : 0;
   a.err = err;
   if (fused) {
     a.k_new = k_new;
@@ -336,7 +340,7 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
   }
   int launches = 0;
   cudaError_t e = use_tc ? launch_decode_tc(a, dtype, s, &launches) : launch_attn_simt(a, dtype, s, &launches);
-  if (e == cudaSuccess && max_parts > 1) {
+  if (e == cudaSuccess && max_parts > 1 && !cluster) {
     MergeArgs m{};
     m.out = out;
     m.part_m = a.ws_m;

@@ -23,6 +23,7 @@
 //
 // The tile loop inside a warp visits tokens in increasing logical order, so the result depends
 // only on logical positions, not on where the blocks sit in the pool.
+#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -58,11 +59,13 @@ struct TcCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;  // K and V
   static constexpr int kStages = D == 128 ? PA_TC_STAGES_128 : PA_TC_STAGES_64;  // per warp
-  static constexpr int kSmemBytes = 1024 /*barriers*/ + 1024 /*alignment*/ + kTcWarps * kStages * kStageBytes;
+  static constexpr int kPartialBytes = (8 * D + 16) * 4;  // one CTA's (acc, max, sum) for up to 8 heads
+  static constexpr int kSmemBytes =
+      1024 /*barriers*/ + 1024 /*alignment*/ + kTcWarps * kStages * kStageBytes + kPartialBytes;
   static_assert(kTcWarps * kStages * 8 <= 1024, "barriers must fit their 1 KB slot");
 };
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool kCluster>
 __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
     decode_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
@@ -79,10 +82,12 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base);
   uint8_t* stages = base + 1024;
 
-  const int kvh = blockIdx.x % a.n_kv_heads;
-  const int64_t rest = blockIdx.x / a.n_kv_heads;
-  const int part = (int)(rest % a.max_parts);
-  const int64_t row = rest / a.max_parts;
+  // grid order: KV heads innermost (CTAs touching one physical block run together), or, for the
+  // cluster merge, partitions innermost (one cluster = the partitions of one (row, KV head))
+  const int kvh = kCluster ? (int)((blockIdx.x / a.max_parts) % a.n_kv_heads) : (int)(blockIdx.x % a.n_kv_heads);
+  const int part = kCluster ? (int)(blockIdx.x % a.max_parts) : (int)((blockIdx.x / a.n_kv_heads) % a.max_parts);
+  const int64_t row = kCluster ? (int64_t)(blockIdx.x / a.max_parts) / a.n_kv_heads
+                               : (int64_t)(blockIdx.x / a.n_kv_heads) / a.max_parts;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int g = lane >> 2;   // mma row group: query head g of the group
@@ -96,9 +101,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
     len = len < 0 ? 0 : max_len;
   }
   const int n_parts_row = len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
-  if (part >= n_parts_row) return;
+  if (!kCluster && part >= n_parts_row) return;
+  const bool active = part < n_parts_row;  // a cluster's surplus CTAs stay for the barriers
   const int64_t t_begin = (int64_t)part * a.part_tokens;
-  const int64_t t_end = min(t_begin + a.part_tokens, len);
+  const int64_t t_end = active ? min(t_begin + a.part_tokens, len) : t_begin;
   const int n_tiles = (int)((t_end - t_begin + kTile - 1) / kTile);
   const int my_tiles = n_tiles > warp ? (n_tiles - warp + kTcWarps - 1) / kTcWarps : 0;
 
@@ -329,7 +335,14 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
       }
     }
     const int64_t qh = row * a.n_q_heads + (int64_t)kvh * G + h;
-    if (direct) {
+    if (kCluster) {
+      float* cp = reinterpret_cast<float*>(stages + kTcWarps * kStages * kStageBytes);
+      cp[h * D + d] = A;
+      if (d == 0) {
+        cp[G * D + h] = M;
+        cp[G * D + G + h] = L;
+      }
+    } else if (direct) {
       static_cast<T*>(a.out)[qh * D + d] = Elt<T>::from_float(L != 0.f ? A / L : 0.f);
     } else {
       const int64_t pi = qh * a.max_parts + part;
@@ -339,6 +352,40 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
         a.ws_l[pi] = L;
       }
     }
+  }
+  if constexpr (kCluster) {
+    // log-sum-exp merge of the cluster's partitions through distributed shared memory: rank 0 reads
+    // every rank's (acc, max, sum) once all are written, the others stay resident until it is done
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (part == 0) {
+      float* cp = reinterpret_cast<float*>(stages + kTcWarps * kStages * kStageBytes);
+      for (int i = threadIdx.x; i < G * D; i += kTcWarps * 32) {
+        const int h = i / D;
+        const int d = i - h * D;
+        float M = -INFINITY;
+        for (int p = 0; p < a.max_parts; ++p) {
+          const float* rp = cluster.map_shared_rank(cp, p);
+          if (rp[G * D + G + h] != 0.f) M = fmaxf(M, rp[G * D + h]);
+        }
+        float L = 0.f, A = 0.f;
+        if (M != -INFINITY) {
+          for (int p = 0; p < a.max_parts; ++p) {
+            const float* rp = cluster.map_shared_rank(cp, p);
+            const float lp = rp[G * D + G + h];
+            if (lp != 0.f) {
+              const float f = fast_exp2(rp[G * D + h] - M);
+              L = fmaf(lp, f, L);
+              A = fmaf(rp[h * D + d], f, A);
+            }
+          }
+        }
+        const int64_t qh = row * a.n_q_heads + (int64_t)kvh * G + h;
+        static_cast<T*>(a.out)[qh * D + d] = Elt<T>::from_float(L != 0.f ? A / L : 0.f);
+      }
+    }
+    cluster.sync();
   }
 }
 
@@ -387,7 +434,7 @@ bool decode_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, i
   return encode_fn() != nullptr;
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool kCluster>
 static cudaError_t launch_tc_g(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
   constexpr int smem = TcCfg<D>::kSmemBytes;
   static bool attr_set[64] = {};  // per instantiation and device; idempotent, so a race is harmless
@@ -395,24 +442,42 @@ static cudaError_t launch_tc_g(const AttnArgs& a, const CUtensorMap& km, const C
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_tc_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(decode_tc_kernel<T, D, G, kCluster>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int64_t grid = a.rows * (int64_t)a.max_parts * a.n_kv_heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  decode_tc_kernel<T, D, G><<<(unsigned)grid, kTcWarps * 32, smem, s>>>(a, km, vm);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kTcWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (kCluster) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)a.max_parts;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, D, G, kCluster>, a, km, vm);
+}
+
+template <typename T, int D, int G>
+static cudaError_t launch_tc_c(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
+  return a.cluster ? launch_tc_g<T, D, G, true>(a, km, vm, s) : launch_tc_g<T, D, G, false>(a, km, vm, s);
 }
 
 template <typename T, int D>
 static cudaError_t launch_tc_d(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
   switch (a.group) {
-    case 1: return launch_tc_g<T, D, 1>(a, km, vm, s);
-    case 2: return launch_tc_g<T, D, 2>(a, km, vm, s);
-    case 4: return launch_tc_g<T, D, 4>(a, km, vm, s);
-    case 8: return launch_tc_g<T, D, 8>(a, km, vm, s);
+    case 1: return launch_tc_c<T, D, 1>(a, km, vm, s);
+    case 2: return launch_tc_c<T, D, 2>(a, km, vm, s);
+    case 4: return launch_tc_c<T, D, 4>(a, km, vm, s);
+    case 8: return launch_tc_c<T, D, 8>(a, km, vm, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -69,6 +69,9 @@ struct AttnArgs {
   const int64_t* slot_mapping;
   void* k_pool_w;                  // the pools again, writable
   void* v_pool_w;
+  // tensor-core decode: 1 = the partitions of a row form one thread-block cluster and merge their
+  // partial states through distributed shared memory (no workspace, no merge kernel)
+  int cluster;
 };
 
 struct MergeArgs {

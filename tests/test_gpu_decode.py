@@ -158,11 +158,12 @@ def _ragged_case(dtype, Hq, Hkv, D, S, lens, seed, NB=None):
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("S", [8, 16, 32])
-@pytest.mark.parametrize("part", [0, 64, "none"])
+@pytest.mark.parametrize("part", [0, 64, 128, "none"])
 @pytest.mark.parametrize("kernel", [0, 1])
 def test_decode_shapes_and_partitions(cuda_lib, dtype, D, G, S, part, kernel):
     """kernel 0 = automatic choice (tensor-core path for bf16/fp16 with block_size % 16 == 0),
-    1 = CUDA-core path forced."""
+    1 = CUDA-core path forced.  part 64 gives 9-19 partitions per row (workspace + merge kernel),
+    part 128 gives 4-9 (thread-block-cluster merge on the tensor-core path when at most 8)."""
     pa = cuda_lib
     pa.set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
     Hkv = 2

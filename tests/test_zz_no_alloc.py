@@ -31,8 +31,10 @@ def _call_static(lib, out, case, q, lens, table):
 def test_static_scratch_decode_matches_workspace_decode_twice(cuda_lib):
     pa = cuda_lib
     lib = pa.load_library()
-    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 0)
-    lens = W.llama_context_lens()  # 512..4096 tokens: split-K with 8 partitions per row
+    # 256-token partitions: 512..4096-token contexts split into up to 16 partitions, more than one
+    # thread-block cluster holds, so the partial states go through the scratch array and the merge
+    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 256)
+    lens = W.llama_context_lens()
     inp = W.device_decode_inputs(lens, n_q_heads=32, n_kv_heads=8, head_dim=128, block_size=16,
                                  dtype=torch.bfloat16, num_blocks=W.LLAMA_POOL,
                                  max_blocks_per_seq=W.LLAMA_MAX_CTX // 16, device="cuda", seed=2024)
@@ -54,6 +56,7 @@ def test_static_scratch_decode_matches_workspace_decode_twice(cuda_lib):
         err = (out.double() - ref.double()).abs().max().item()
         assert err <= 2e-2, f"call {call}: max abs err {err}"
     assert pa.device_error_flags() == 0
+    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 0)
 
 
 def test_static_scratch_rejects_problems_larger_than_the_array(cuda_lib):
