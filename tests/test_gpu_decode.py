@@ -282,6 +282,7 @@ def test_both_kernels_agree_on_the_serving_shape(cuda_lib, kernel):
 
 def test_workspace_too_small_is_rejected(cuda_lib):
     pa = cuda_lib
+    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 128)  # 16 partitions: more than a cluster merges, workspace needed
     case = _ragged_case(torch.bfloat16, 8, 2, 64, 16, [2000], seed=10)
     with pytest.raises(pa.PagedAttnError) as ei:
         pa.paged_attention_decode(case.q.cuda(), case.k_pool.cuda(), case.v_pool.cuda(),
