@@ -156,6 +156,9 @@ int pa_set_option(int option, int64_t value) {
     case PA_OPT_PARTITION_TOKENS:
       if (value < 0 || value > (int64_t(1) << 30)) return PA_EINVAL;
       break;
+    case PA_OPT_CLUSTER_MERGE:
+      if (value != 0 && value != 1) return PA_EINVAL;
+      break;
     default:
       return PA_EINVAL;
   }
@@ -164,7 +167,7 @@ int pa_set_option(int option, int64_t value) {
 }
 
 int64_t pa_get_option(int option) {
-  if (option < 1 || option > 4) return PA_EINVAL;
+  if (option < 1 || option > 5) return PA_EINVAL;
   return g_options[option].load();
 }
 
@@ -293,7 +296,7 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
   WsLayout ws = workspace_layout((int64_t)batch * n_q_heads, max_parts, head_dim);
   // up to 8 partitions per row on the tensor-core path: one thread-block cluster per row merges
   // through distributed shared memory, with neither workspace nor merge kernel
-  const bool cluster = use_tc && max_parts >= 2 && max_parts <= 8;
+  const bool cluster = use_tc && max_parts >= 2 && max_parts <= 8 && g_options[PA_OPT_CLUSTER_MERGE].load() != 0;
   if (max_parts > 1 && !cluster) {
     if (workspace == nullptr) {
       max_parts = 1;

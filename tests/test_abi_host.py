@@ -51,6 +51,8 @@ def test_options_validate(lib):
     assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 256) == 0
     assert lib.pa_get_option(pa.PA_OPT_PARTITION_TOKENS) == 256
     assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 0) == 0
+    assert lib.pa_set_option(pa.PA_OPT_CLUSTER_MERGE, 2) == pa.PA_EINVAL
+    assert lib.pa_get_option(pa.PA_OPT_CLUSTER_MERGE) == 0
 
 
 def test_argument_errors_are_returned_before_any_launch(lib):

@@ -36,6 +36,7 @@ def _reset_options(cuda_lib):
     pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 0)
     pa.set_option(pa.PA_OPT_DECODE_KERNEL, 0)
     pa.set_option(pa.PA_OPT_CHECKED, 0)
+    pa.set_option(pa.PA_OPT_CLUSTER_MERGE, 0)
     pa.device_error_flags(clear=True)
 
 
@@ -158,14 +159,18 @@ def _ragged_case(dtype, Hq, Hkv, D, S, lens, seed, NB=None):
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("S", [8, 16, 32])
-@pytest.mark.parametrize("part", [0, 64, 128, "none"])
+@pytest.mark.parametrize("part", [0, 64, 128, "none", "cluster"])
 @pytest.mark.parametrize("kernel", [0, 1])
 def test_decode_shapes_and_partitions(cuda_lib, dtype, D, G, S, part, kernel):
     """kernel 0 = automatic choice (tensor-core path for bf16/fp16 with block_size % 16 == 0),
-    1 = CUDA-core path forced.  part 64 gives 9-19 partitions per row (workspace + merge kernel),
-    part 128 gives 4-9 (thread-block-cluster merge on the tensor-core path when at most 8)."""
+    1 = CUDA-core path forced.  part 64 gives 9-19 partitions per row, 128 gives 4-9 (workspace +
+    merge kernel); "cluster" = 128-token partitions with the thread-block-cluster merge switched on
+    (used on the tensor-core path when a row has at most 8 partitions)."""
     pa = cuda_lib
     pa.set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
+    if part == "cluster":
+        pa.set_option(pa.PA_OPT_CLUSTER_MERGE, 1)
+        part = 128
     Hkv = 2
     lens = [0, 1, S - 1, S, S + 1, 3 * S + 5, 200, 517]  # history before the new token
     case = _ragged_case(dtype, Hkv * G, Hkv, D, S, lens, seed=D * 31 + G * 7 + S)
