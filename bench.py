@@ -302,7 +302,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=4, help="independent layer pools rotated over the steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--partition-tokens", type=int, default=0, help="split-K partition length (0 = library default)")
     ap.add_argument("--decode-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
@@ -415,36 +415,66 @@ def main():
     if pa.device_error_flags() != 0:
         raise RuntimeError("device error word set during the benchmark")
 
-    # end to end through the C ABI with pinned host buffers: inputs in, output out, every step
+    # end to end through the C ABI with pinned host buffers: every step copies its inputs (queries,
+    # new K/V, slots, tables, lengths) host -> device and its output device -> host.  Two buffer sets
+    # and three streams let step i + 1's upload and step i - 1's download run under step i's kernels.
     e2e = None
     E = args.e2e_steps
     if E > 0:
-        host = {k: t.cpu().pin_memory() for k, t in dict(q=q, kn=kn, vn=vn, slot=slot, table=table, ctx=ctx).items()}
-        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        names = ("q", "kn", "vn", "slot", "table", "ctx")
+        src = dict(q=q, kn=kn, vn=vn, slot=slot, table=table, ctx=ctx)
+        host = {k: src[k].cpu().pin_memory() for k in names}
+        host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        sets = [{k: torch.empty_like(src[k]) for k in names} for _ in range(2)]
+        for st_ in sets:
+            st_["out"] = torch.empty_like(out)
         h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = host_out.numel() * host_out.element_size()
-        devs = dict(q=q, kn=kn, vn=vn, slot=slot, table=table, ctx=ctx)
+        d2h = host_out[0].numel() * host_out[0].element_size()
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        freed = [torch.cuda.Event() for _ in range(2)]
 
         def e2e_step(i):
-            for k in host:
-                devs[k].copy_(host[k], non_blocking=True)
-            step_pre(i % args.layers)
-            step_main(i % args.layers)
-            host_out.copy_(out, non_blocking=True)
+            j = i & 1
+            bufs = sets[j]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(freed[j])
+                for k in names:
+                    bufs[k].copy_(host[k], non_blocking=True)
+                in_ready[j].record(s_in)
+            stream.wait_event(in_ready[j])
+            kp, vp = pools[i % args.layers]
+            st = lib.paged_attention_decode_fused(bufs["out"].data_ptr(), bufs["q"].data_ptr(), bufs["kn"].data_ptr(),
+                                                  bufs["vn"].data_ptr(), bufs["slot"].data_ptr(), kp.data_ptr(),
+                                                  vp.data_ptr(), bufs["table"].data_ptr(), bt_stride,
+                                                  bufs["ctx"].data_ptr(), B, W.LLAMA_POOL, S, scale, HQ, HKV, D,
+                                                  pa.PA_BF16, ptr["ws"], ws_bytes, sp)
+            if st:
+                raise RuntimeError(f"paged_attention_decode_fused status {st}")
+            done[j].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done[j])
+                host_out[j].copy_(bufs["out"], non_blocking=True)
+                freed[j].record(s_out)
 
-        for i in range(3):
+        for i in range(4):
             e2e_step(i)
+        torch.cuda.synchronize()
         barrier(dist)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e0.record(s_in)
         for i in range(E):
             e2e_step(i)
-        e1.record(stream)
+        e1.record(s_out)
         torch.cuda.synchronize()
         barrier(dist)
         e_ms = max_over_ranks(e0.elapsed_time(e1), dist)
         e2e = {"value": step_bytes * E * world / (e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / E}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / E,
+               "api": "paged_attention_decode_fused through the C ABI, pinned host buffers, copies overlapped "
+                      "with the previous/next step on two copy streams"}
 
     if rank != 0:
         if dist is not None:

@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
   }
   const float* pm = a.part_m + row * a.n_parts;
   const float* pl = a.part_l + row * a.n_parts;
+  const float* pacc = a.part_acc + row * a.n_parts * (int64_t)D + lane * kPer;
+  // the row maximum over partitions that hold tokens: lane p looks at partitions p, p + 32, ...
   float M = -INFINITY;
   for (int p = lane; p < parts; p += 32)
     if (pl[p] != 0.f) M = fmaxf(M, pm[p]);
@@ -43,25 +45,37 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
 #pragma unroll
   for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
   if (M != -INFINITY) {
-    const float* pa_ = a.part_acc + row * a.n_parts * (int64_t)D + lane * kPer;
-    for (int p = 0; p < parts; ++p) {
-      const float lp = pl[p];
-      if (lp == 0.f) continue;
-      const float f = fast_exp2(pm[p] - M);
-      L = fmaf(lp, f, L);
+    for (int p0 = 0; p0 < parts; p0 += 32) {
+      // weight of partition p0 + lane, then every lane accumulates its head_dim slice over the chunk
+      const int p = p0 + lane;
+      float w = 0.f;
+      if (p < parts) {
+        const float lp = pl[p];
+        if (lp != 0.f) {
+          w = fast_exp2(pm[p] - M);
+          L = fmaf(lp, w, L);
+        }
+      }
+      const int n = parts - p0 < 32 ? parts - p0 : 32;
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, j);
+        if (wj != 0.f) {
+          const float* src = pacc + (int64_t)(p0 + j) * D;
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) acc[i] = fmaf(pa_[(int64_t)p * D + i], f, acc[i]);
+          for (int i = 0; i < kPer; ++i) acc[i] = fmaf(src[i], wj, acc[i]);
+        }
+      }
     }
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   const float inv = L != 0.f ? 1.f / L : 0.f;
   T* o = static_cast<T*>(a.out) + row * D + lane * kPer;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) o[i] = Elt<T>::from_float(acc[i] * inv);
 }
 
-// Launched with programmatic stream serialization when it follows a partition kernel in the same
-// call: its CTAs may be scheduled while the partition grid drains and then wait (griddepcontrol) for
-// that grid's completion, which hides the launch gap between the two kernels.
 template <typename T, int D>
 static cudaError_t launch_merge_d(const MergeArgs& a, cudaStream_t s, unsigned blocks, bool pdl) {
   cudaLaunchConfig_t cfg = {};
