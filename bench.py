@@ -35,6 +35,10 @@ UNIT = "GB/s"
 HQ, HKV, D, S = 32, 8, 128, 16
 LLAMA_LAYERS = 32
 ELT = 2  # bf16
+# dram__bytes_read.sum + dram__bytes_write.sum of one paged_attention_decode_fused call on this
+# workload (partition kernel 578.7 + 5.7 MB, merge kernel 2.5 MB), from the ncu capture summarised in
+# profiles/decode_fused_llama3_8b_serving.md.  Retake it whenever either kernel changes.
+FUSED_CALL_DRAM_BYTES = 586.9e6
 
 
 def measured_peaks():
@@ -507,7 +511,10 @@ def main():
                      "kernel": ("paged_attention_decode_fused (write + partition kernel, then merge kernel)" if use_fused
                                 else "paged_attention_decode (partition + merge kernels)"),
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None},
+                     "frac": achieved / peak,
+                     # DRAM bytes of one fused call (both kernels) from the ncu capture summarised in
+                     # profiles/decode_fused_llama3_8b_serving.md; None for the two-call variant
+                     "traffic": FUSED_CALL_DRAM_BYTES if use_fused else None},
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,
