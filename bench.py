@@ -122,18 +122,31 @@ def dist_setup(n_gpus: int):
     return 0, 1, 0, None
 
 
-def barrier(dist):
+def barrier(dist, cuda: bool = True):
     if dist is not None:
         dist.barrier()
-    torch.cuda.synchronize()
+    if cuda:
+        torch.cuda.synchronize()
 
 
-def max_over_ranks(x: float, dist) -> float:
+def max_over_ranks(x: float, dist, device: str = "cuda") -> float:
+    """The slowest rank's time: every replica's timed region counts in full."""
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_seed(rank: int) -> int:
+    """Each replica draws its own device inputs (same shapes, different values)."""
+    return W.SEED_BASE + 3 + 1000 * rank
+
+
+def whole_job_gbs(step_bytes: float, steps: int, world: int, slowest_ms: float) -> float:
+    """Weak scaling: every replica moves step_bytes per step; the job's throughput is all replicas'
+    bytes over the slowest replica's time."""
+    return step_bytes * steps * world / (slowest_ms * 1e-3) / 1e9
 
 
 def cpu_baseline(budget_s: float = 10.0):
@@ -336,7 +349,7 @@ def main():
     inp = W.device_decode_inputs(lens, n_q_heads=HQ, n_kv_heads=HKV, head_dim=D, block_size=S,
                                  dtype=torch.bfloat16, num_blocks=W.LLAMA_POOL,
                                  max_blocks_per_seq=W.LLAMA_MAX_CTX // S, device=dev,
-                                 seed=W.SEED_BASE + 3 + 1000 * rank, layers=args.layers)
+                                 seed=replica_seed(rank), layers=args.layers)
     table = inp["block_table"].to(dev)
     ctx = inp["context_lens"].to(dev)
     slot = inp["slot_mapping"].to(dev)
@@ -418,7 +431,7 @@ def main():
     kvb, wb = algorithmic_bytes(lens, B)
     step_bytes = kvb + wb
     ms_per_step = total_ms / K
-    value = step_bytes * K * world / (total_ms * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, K, world, total_ms)
     peak, peak_kind = measured_peaks()
     achieved = (step_bytes if use_fused else kvb) / (dec_ms * 1e-3) / 1e9
     if pa.device_error_flags() != 0:
@@ -480,7 +493,7 @@ def main():
         torch.cuda.synchronize()
         barrier(dist)
         e_ms = max_over_ranks(e0.elapsed_time(e1), dist)
-        e2e = {"value": step_bytes * E * world / (e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": whole_job_gbs(step_bytes, E, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / E,
                "api": "paged_attention_decode_fused through the C ABI, pinned host buffers, copies overlapped "
                       "with the previous/next step on two copy streams"}
