@@ -311,6 +311,71 @@ def run_prefill(args):
     return 0
 
 
+def run_swap(args):
+    """Block swap between the device pool and a pinned host pool (the offload tier): 8192 blocks of the
+    serving shape (32 KB of K and 32 KB of V each, 512 MB per direction) swapped out, then swapped
+    back in to other physical blocks, one swap_blocks call per direction."""
+    import pagedattention_kv_cache_paged_gb300 as pa
+    lib = pa.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    NB, NH = W.LLAMA_POOL, 8192
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(W.SEED_BASE + 6)
+    kp = torch.randn((NB, S, HKV, D), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    vp = torch.randn((NB, S, HKV, D), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    hk = torch.empty((NH, S, HKV, D), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty((NH, S, HKV, D), dtype=torch.bfloat16).pin_memory()
+    hgen = torch.Generator().manual_seed(W.SEED_BASE + 6)
+    perm = torch.randperm(NB, generator=hgen)
+    out_pairs = torch.stack([perm[:NH], torch.arange(NH)], dim=1).to(torch.int64).to(dev)
+    in_pairs = torch.stack([torch.arange(NH), perm[NH:2 * NH]], dim=1).to(torch.int64).to(dev)
+    block_bytes = S * HKV * D * ELT
+    moved = NH * block_bytes * 2  # K and V
+
+    def swap(dst, src, pairs, ndst, nsrc):
+        st = lib.swap_blocks(dst[0].data_ptr(), dst[1].data_ptr(), ndst, src[0].data_ptr(), src[1].data_ptr(),
+                             nsrc, pairs.data_ptr(), NH, block_bytes, sp)
+        if st:
+            raise RuntimeError(f"swap_blocks status {st}")
+
+    for _ in range(args.warmup):
+        swap((hk, hv), (kp, vp), out_pairs, NH, NB)
+        swap((kp, vp), (hk, hv), in_pairs, NB, NH)
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    t_out, t_in = 0.0, 0.0
+    clocks = ClockSampler(0)
+    clocks.start()
+    launches0 = pa.launch_count()
+    for _ in range(K):
+        ev[0].record(stream)
+        swap((hk, hv), (kp, vp), out_pairs, NH, NB)
+        ev[1].record(stream)
+        swap((kp, vp), (hk, hv), in_pairs, NB, NH)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        t_out += ev[0].elapsed_time(ev[1])
+        t_in += ev[1].elapsed_time(ev[2])
+    clk = clocks.stop()
+    launches = pa.launch_count() - launches0
+    if pa.device_error_flags() != 0:
+        raise RuntimeError("device error word set during the benchmark")
+    line = {"metric": "paged block swap: GB/s between the device pool and a pinned host pool",
+            "value": 2 * moved * K / ((t_out + t_in) * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1, "steps": K,
+            "warmup": args.warmup, "ms_per_step": (t_out + t_in) / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "swap_blocks: 8192 blocks x (32 KB K + 32 KB V) device -> pinned host, then "
+                                   "host -> device into other blocks (Llama-3-8B pool shape)",
+                       "bytes_per_direction": moved},
+            "swap_out_gbs": moved * K / (t_out * 1e-3) / 1e9, "swap_in_gbs": moved * K / (t_in * 1e-3) / 1e9,
+            "gpu_launches": launches, "clocks": clk}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -322,7 +387,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--partition-tokens", type=int, default=0, help="split-K partition length (0 = library default)")
     ap.add_argument("--decode-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
-    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
+    ap.add_argument("--workload", choices=["decode", "prefill", "swap"], default="decode")
     ap.add_argument("--unfused", action="store_true",
                     help="time paged_kv_write + paged_attention_decode as two calls instead of the fused call")
     ap.add_argument("--prefill-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05, 3 mma.sync")
@@ -331,6 +396,8 @@ def main():
         return run_reference(args)
     if args.workload == "prefill":
         return run_prefill(args)
+    if args.workload == "swap":
+        return run_swap(args)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 

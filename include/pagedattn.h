@@ -187,6 +187,25 @@ PA_API int copy_blocks(void* k_pool, void* v_pool, const int64_t* block_pairs, i
                 int64_t num_blocks, int64_t block_bytes, void* stream);
 
 /*
+ * swap_blocks — move blocks between two pools in one launch: the device pool and a pinned host pool
+ * (Pico-vLLM dev log #5 "Paged Attention", core data structures: swap_out copies GPU blocks to the
+ * pinned CPU pool, swap_in copies them back; the table and free-list bookkeeping stay with the
+ * caller), or two device pools.
+ *   dst_k_pool, dst_v_pool  destination pools, dst_num_blocks blocks each
+ *   src_k_pool, src_v_pool  source pools, src_num_blocks blocks each
+ *   Each pool is device memory or pinned host memory (cudaHostAlloc / cudaHostRegister, reachable
+ *   from the device); pageable host memory returns PA_EINVAL.
+ *   block_pairs  int64 [n_pairs][2] = (src block, dst block), device memory or pinned host memory.
+ *                A dst must not appear twice (checked mode rejects it); out-of-range ids are
+ *                skipped on the device and recorded as PA_DEVERR_COPY_PAIR.
+ *   block_bytes  bytes of one block of one pool (block_size * n_kv_heads * head_dim * element size),
+ *                a multiple of 16.  The copy is bit-exact and ordered on `stream`.
+ */
+PA_API int swap_blocks(void* dst_k_pool, void* dst_v_pool, int64_t dst_num_blocks, const void* src_k_pool,
+                       const void* src_v_pool, int64_t src_num_blocks, const int64_t* block_pairs, int64_t n_pairs,
+                       int64_t block_bytes, void* stream);
+
+/*
  * paged_attention_lse_merge — merge split-K partials exactly (the partition-combining identity of
  * the online softmax in JuliaPagedAttn README "Online Softmax", applied to whole partitions).
  *   part_max   fp32 [rows][n_parts]   running maxima in the log2 domain (score * log2(e))

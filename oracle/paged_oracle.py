@@ -310,3 +310,14 @@ def copy_blocks(k_pool, v_pool, pairs):
         kp[int(dst)] = kp[int(src)]
         vp[int(dst)] = vp[int(src)]
     return kp, vp
+
+
+def transfer_blocks(dst_k, dst_v, src_k, src_v, pairs):
+    """Block swap between two pools (Pico-vLLM dev log #5 "Paged Attention", swap_out / swap_in): for
+    each ``(src, dst)`` pair, block ``dst`` of the destination pools becomes a bit copy of block
+    ``src`` of the source pools.  Returns new destination pools."""
+    kd, vd = dst_k.clone(), dst_v.clone()
+    for src, dst in to_int(pairs).reshape(-1, 2):
+        kd[int(dst)] = src_k[int(src)]
+        vd[int(dst)] = src_v[int(src)]
+    return kd, vd

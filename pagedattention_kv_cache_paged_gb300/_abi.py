@@ -39,6 +39,7 @@ SIGNATURES = {
     "paged_attention_prefill": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _i32, _i64, _i32, _f32,
                                        _i32, _i32, _i32, _i32, _vp]),
     "copy_blocks": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "swap_blocks": (_i32, [_vp, _vp, _i64, _vp, _vp, _i64, _vp, _i64, _i64, _vp]),
     "paged_attention_lse_merge": (_i32, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp]),
     "paged_attention_decode_static_scratch": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _i64, _i32, _f32,
                                                      _i32, _i32, _i32, _i32, _vp]),
@@ -303,6 +304,29 @@ def copy_blocks(k_pool, v_pool, block_pairs, stream=None):
                          _dev(block_pairs, "block_pairs", torch.int64) if n else None, n, NB, block_bytes,
                          _stream(stream))
     _check("copy_blocks", st)
+
+
+def swap_blocks(dst_k_pool, dst_v_pool, src_k_pool, src_v_pool, block_pairs, stream=None):
+    """Copy block ``src`` of the source pools to block ``dst`` of the destination pools for every
+    ``(src, dst)`` row of int64 ``block_pairs [n, 2]``.  Pools may be CUDA tensors or pinned CPU
+    tensors (``pin_memory()``); ``block_pairs`` a CUDA tensor or a pinned CPU tensor."""
+    lib = load_library()
+    if dst_k_pool.shape[1:] != src_k_pool.shape[1:] or dst_k_pool.dtype != src_k_pool.dtype:
+        raise ValueError("source and destination pools must share block shape and dtype")
+    for name, t in (("dst_k_pool", dst_k_pool), ("dst_v_pool", dst_v_pool), ("src_k_pool", src_k_pool),
+                    ("src_v_pool", src_v_pool), ("block_pairs", block_pairs)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    n = int(block_pairs.shape[0]) if block_pairs.numel() else 0
+    if block_pairs.dtype != torch.int64 or (n and (block_pairs.dim() != 2 or block_pairs.shape[1] != 2)):
+        raise ValueError("block_pairs must be int64 [n, 2]")
+    block_bytes = int(src_k_pool[0].numel()) * src_k_pool.element_size()
+    st = lib.swap_blocks(dst_k_pool.data_ptr(), dst_v_pool.data_ptr(), int(dst_k_pool.shape[0]),
+                         src_k_pool.data_ptr(), src_v_pool.data_ptr(), int(src_k_pool.shape[0]),
+                         block_pairs.data_ptr() if n else None, n, block_bytes, _stream(stream))
+    _check("swap_blocks", st)
 
 
 def paged_attention_lse_merge(part_max, part_sum, part_acc, out_dtype=torch.bfloat16, out=None, stream=None):

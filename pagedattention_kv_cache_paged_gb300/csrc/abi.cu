@@ -477,6 +477,71 @@ int copy_blocks(void* k_pool, void* v_pool, const int64_t* block_pairs, int64_t 
   return finish(e, launches);
 }
 
+// Device-accessible address of a pool: device memory as is, pinned host memory through its mapping.
+static int device_address(const void* p, void** out) {
+  cudaPointerAttributes at{};
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return PA_EINVAL;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+    *out = const_cast<void*>(p);
+    return PA_OK;
+  }
+  if (at.type == cudaMemoryTypeHost && at.devicePointer != nullptr) {
+    *out = at.devicePointer;
+    return PA_OK;
+  }
+  return PA_EINVAL;  // pageable host memory: not reachable from the device
+}
+
+int swap_blocks(void* dst_k_pool, void* dst_v_pool, int64_t dst_num_blocks, const void* src_k_pool,
+                const void* src_v_pool, int64_t src_num_blocks, const int64_t* block_pairs, int64_t n_pairs,
+                int64_t block_bytes, void* stream) {
+  if (n_pairs < 0 || dst_num_blocks <= 0 || src_num_blocks <= 0 || block_bytes <= 0 || block_bytes % 16 != 0)
+    return PA_EINVAL;
+  if (n_pairs == 0) return PA_OK;
+  if (!dst_k_pool || !dst_v_pool || !src_k_pool || !src_v_pool || !block_pairs) return PA_EINVAL;
+  if (!aligned16(dst_k_pool) || !aligned16(dst_v_pool) || !aligned16(src_k_pool) || !aligned16(src_v_pool))
+    return PA_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned* err = nullptr;
+  int rc = device_info(&err, nullptr);
+  if (rc) return rc;
+  SwapArgs a{};
+  void* p = nullptr;
+  if ((rc = device_address(dst_k_pool, &p))) return rc;
+  a.dst_k = p;
+  if ((rc = device_address(dst_v_pool, &p))) return rc;
+  a.dst_v = p;
+  if ((rc = device_address(src_k_pool, &p))) return rc;
+  a.src_k = p;
+  if ((rc = device_address(src_v_pool, &p))) return rc;
+  a.src_v = p;
+  if ((rc = device_address(block_pairs, &p))) return rc;
+  a.pairs = static_cast<const int64_t*>(p);
+  if (checked()) {
+    std::vector<int64_t> pairs;
+    rc = copy_to_host(pairs, a.pairs, 2 * n_pairs, s);
+    if (rc) return rc;
+    std::unordered_set<int64_t> dsts;
+    for (int64_t i = 0; i < n_pairs; ++i) {
+      const int64_t src = pairs[(size_t)(2 * i)], dst = pairs[(size_t)(2 * i + 1)];
+      if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) return PA_ERANGE;
+      if (!dsts.insert(dst).second) return PA_ERANGE;
+    }
+  }
+  a.n_pairs = n_pairs;
+  a.src_num_blocks = src_num_blocks;
+  a.dst_num_blocks = dst_num_blocks;
+  a.block_vecs = block_bytes / 16;
+  a.err = err;
+  int launches = 0;
+  cudaError_t e = launch_swap_blocks(a, s, &launches);
+  return finish(e, launches);
+}
+
 int paged_attention_lse_merge(void* out, const float* part_max, const float* part_sum,
                               const float* part_acc, int64_t rows, int n_parts, int head_dim,
                               pa_dtype dtype, void* stream) {

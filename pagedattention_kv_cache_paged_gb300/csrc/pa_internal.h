@@ -34,6 +34,20 @@ struct CopyBlocksArgs {
   unsigned* err;
 };
 
+// Block transfer between two pools (either may be mapped pinned host memory).
+struct SwapArgs {
+  void* dst_k;
+  void* dst_v;
+  const void* src_k;
+  const void* src_v;
+  const int64_t* pairs;  // (src, dst)
+  int64_t n_pairs;
+  int64_t src_num_blocks;
+  int64_t dst_num_blocks;
+  int64_t block_vecs;    // block_bytes / 16
+  unsigned* err;
+};
+
 // One attention launch over "rows": a decode row is a sequence, a prefill row is a query token.
 struct AttnArgs {
   void* out;
@@ -94,6 +108,7 @@ struct MergeArgs {
 // Launchers: return cudaSuccess or the launch error.  `launches` is incremented per kernel.
 cudaError_t launch_kv_write(const KvWriteArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
 cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t s, int* launches);
+cudaError_t launch_swap_blocks(const SwapArgs& a, cudaStream_t s, int* launches);
 cudaError_t launch_attn_simt(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
 cudaError_t launch_lse_merge(const MergeArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
 

@@ -401,3 +401,16 @@ def test_sampled_rows_equal_full_decode():
                                     t["scale"], [(0, 1), (1, 0)])
     assert np.array_equal(rows[(0, 1)], full[0, 4:8])
     assert np.array_equal(rows[(1, 0)], full[1, 0:4])
+
+
+def test_transfer_blocks_between_pools():
+    gen = torch.Generator().manual_seed(10)
+    src_k = torch.randn((5, 4, 2, 8), generator=gen).to(torch.bfloat16)
+    src_v = torch.randn((5, 4, 2, 8), generator=gen).to(torch.bfloat16)
+    dst_k = torch.zeros((7, 4, 2, 8), dtype=torch.bfloat16)
+    dst_v = torch.zeros((7, 4, 2, 8), dtype=torch.bfloat16)
+    kd, vd = oracle.transfer_blocks(dst_k, dst_v, src_k, src_v, torch.tensor([[4, 0], [0, 6], [4, 3]]))
+    assert torch.equal(kd[0], src_k[4]) and torch.equal(vd[6], src_v[0]) and torch.equal(kd[3], src_k[4])
+    for blk in (1, 2, 4, 5):
+        assert not kd[blk].float().abs().sum() and not vd[blk].float().abs().sum()
+    assert not dst_k.float().abs().sum()  # inputs untouched
