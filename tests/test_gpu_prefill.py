@@ -200,3 +200,28 @@ def test_prefill_cow_fork_full(cuda_lib):
         q = oracle.to_f64(case.q[qsl[b]:qsl[b + 1]])
         ref = oracle.causal_attention_contiguous(q, oracle.to_f64(k_l), oracle.to_f64(v_l), case.scale)
         assert_close(out[qsl[b]:qsl[b + 1]][rows], ref[rows], torch.bfloat16, f"cow full seq {b}")
+
+
+@pytest.mark.parametrize("kernel", [0, 1, 3])
+def test_mixed_decode_and_prefill_batch(cuda_lib, kernel):
+    """The continuous-batching step: decode rows (1-query chunks at the last position) and prefill
+    chunks of any length in one paged_attention_prefill launch; the decode rows also agree with
+    paged_attention_decode on the same sequences."""
+    pa = cuda_lib
+    hist = [700, 0, 95, 1500, 33, 260, 1023]
+    chunk = [1, 128, 1, 1, 64, 1, 200]
+    case = W.varlen_prefill(99, hist_lens=hist, chunk_lens=chunk, block_size=16, n_q_heads=32, n_kv_heads=8,
+                            head_dim=128, dtype=torch.bfloat16, num_blocks=400)
+    out, dk, dv = run_case(pa, case, kernel=kernel)
+    kp, vp = oracle_pools(case)
+    res = oracle.paged_prefill(case.q, case.query_start_loc, kp, vp, case.block_table, case.context_lens, case.scale)
+    idx = sorted(res)
+    assert_close(out[idx], np.stack([res[i] for i in idx]), torch.bfloat16, f"mixed k{kernel}")
+    # decode rows through the decode kernel
+    qsl = case.query_start_loc.tolist()
+    dec = [b for b, m in enumerate(chunk) if m == 1]
+    qd = torch.stack([case.q[qsl[b]] for b in dec])
+    od = pa.paged_attention_decode(qd.cuda(), dk, dv, case.block_table[dec].contiguous().cuda(),
+                                   case.context_lens[dec].cuda(), case.scale).cpu()
+    for i, b in enumerate(dec):
+        assert (od[i].double() - out[qsl[b]].double()).abs().max().item() <= 2e-2
