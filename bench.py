@@ -36,9 +36,9 @@ HQ, HKV, D, S = 32, 8, 128, 16
 LLAMA_LAYERS = 32
 ELT = 2  # bf16
 # dram__bytes_read.sum + dram__bytes_write.sum of one paged_attention_decode_fused call on this
-# workload (partition kernel 578.7 + 5.7 MB, merge kernel 2.5 MB), from the ncu capture summarised in
-# profiles/decode_fused_llama3_8b_serving.md.  Retake it whenever either kernel changes.
-FUSED_CALL_DRAM_BYTES = 586.9e6
+# workload with separate pools (partition kernel 578.7 + 5.9 MB, merge kernel 2.5 MB), from one
+# `ncu --set full` capture of the fused call.  Retake it whenever either kernel changes.
+FUSED_CALL_DRAM_BYTES = 587.1e6
 
 
 def measured_peaks():
@@ -391,6 +391,8 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="time paged_kv_write + paged_attention_decode as two calls instead of the fused call")
     ap.add_argument("--prefill-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05, 3 mma.sync")
+    ap.add_argument("--kv-layout", choices=["separate", "unified"], default="separate",
+                    help="separate K and V pools, or one pool of unified K/V blocks")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -428,6 +430,16 @@ def main():
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     scale = 1.0 / math.sqrt(D)
     pools = inp["pools"]
+    if args.kv_layout == "unified":
+        pa.set_option(pa.PA_OPT_KV_LAYOUT, pa.KV_LAYOUT_UNIFIED)
+        unified = []
+        for i in range(len(pools)):
+            kp, vp = pools[i]
+            pools[i] = None
+            u = torch.stack([kp, vp], dim=1)
+            del kp, vp
+            unified.append(u)
+            pools[i] = pa.unified_views(u)
     ptr = {k: v.data_ptr() for k, v in dict(table=table, ctx=ctx, slot=slot, q=q, kn=kn, vn=vn, out=out,
                                             ws=ws).items()}
 
@@ -582,7 +594,8 @@ def main():
                          f"{kvb / 1e6:.0f} MB of K/V read per step",
                    "parallelism": f"replicas x{world}",
                    "partition_tokens": args.partition_tokens or 1024,
-                   "decode_kernel": ["auto", "cuda-core", "tensor-core"][args.decode_kernel]},
+                   "decode_kernel": ["auto", "cuda-core", "tensor-core"][args.decode_kernel],
+                   "kv_layout": args.kv_layout},
         "pct_hbm_measured": value / peak,
         "pct_hbm_spec_8000": value / 8000.0,
         "decode_tok_s_attention_only": B * world / (LLAMA_LAYERS * ms_per_step * 1e-3),
@@ -592,9 +605,9 @@ def main():
                                 else "paged_attention_decode (partition + merge kernels)"),
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak,
-                     # DRAM bytes of one fused call (both kernels) from the ncu capture summarised in
-                     # profiles/decode_fused_llama3_8b_serving.md; None for the two-call variant
-                     "traffic": FUSED_CALL_DRAM_BYTES if use_fused else None},
+                     # DRAM bytes of one fused call (both kernels) from the ncu capture; None for the
+                     # two-call variant and for the unified layout (not captured)
+                     "traffic": FUSED_CALL_DRAM_BYTES if use_fused and args.kv_layout == "separate" else None},
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,

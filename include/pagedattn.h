@@ -18,6 +18,16 @@
  *   the device cache tensor is indexed block, token-in-block, kv head, head dim; JuliaPagedAttn
  *   README, "Block Layout": a block holds block_size consecutive tokens for every KV head).
  *   Pool base pointers must be 16-byte aligned.
+ * Unified K/V blocks.  With pa_set_option(PA_OPT_KV_LAYOUT, 1) there is one pool
+ *   [num_blocks][2][block_size][n_kv_heads][head_dim]: physical block b holds the keys of its
+ *   block_size tokens followed by their values, so one table and one allocation serve both
+ *   (JuliaPagedAttn README, "Features": unified K/V blocks, keys and values of a token in one
+ *   block, a single block table and pool).  Every call keeps its k_pool / v_pool pair: k_pool is
+ *   the pool's base and v_pool must be k_pool + block_size * n_kv_heads * head_dim * element size
+ *   (the V half of block 0); any other v_pool returns PA_EINVAL.  Slots, tables, block ids and
+ *   results are the same as with separate pools; only the distance between consecutive blocks of
+ *   the K (or V) view doubles.  The layout is a process-wide setting: change it only between
+ *   calls, never while kernels of another layout are in flight on pools the caller reuses.
  * Slots.  Logical position j of sequence b lives in slot
  *   block_table[b * block_table_stride + j / block_size] * block_size + j % block_size,
  *   i.e. row `slot` of the pool viewed as [num_blocks * block_size][n_kv_heads][head_dim].
@@ -85,11 +95,13 @@ enum {
   PA_OPT_PARTITION_TOKENS = 3, /* 0 auto (default: 1024) or split-K partition length in tokens, rounded up to block_size */
   PA_OPT_PREFILL_KERNEL = 4,   /* 0 auto (default), 1 CUDA-core kernel, 2 tcgen05 tensor-core kernel,
                                   3 mma.sync tensor-core kernel */
-  PA_OPT_CLUSTER_MERGE = 5     /* 0 (default) or 1: on the tensor-core decode path, rows split into 2-8
+  PA_OPT_CLUSTER_MERGE = 5,    /* 0 (default) or 1: on the tensor-core decode path, rows split into 2-8
                                   partitions merge inside one thread-block cluster (distributed shared
                                   memory) instead of the workspace + merge kernel.  Off by default: a
                                   cluster keeps all its CTAs resident until its longest partition ends,
                                   which cost 20 % at the serving shape */
+  PA_OPT_KV_LAYOUT = 6         /* pool layout of every call: 0 (default) separate K and V pools (see
+                                  "Pools"); 1 unified K/V blocks (see "Unified K/V blocks") */
 };
 
 /*
@@ -181,7 +193,8 @@ PA_API int paged_attention_prefill(void* out, const void* q, const int32_t* quer
  * "cow_fork!".
  *   block_pairs  int64 [n_pairs][2] = (src, dst).  A dst must not appear twice nor as a src of
  *                another pair (checked mode rejects both); block_bytes = block_size * n_kv_heads *
- *                head_dim * element size, a multiple of 16.
+ *                head_dim * element size, a multiple of 16 (the bytes of one K half; with unified
+ *                K/V blocks v_pool = k_pool + block_bytes and blocks lie 2 * block_bytes apart).
  */
 PA_API int copy_blocks(void* k_pool, void* v_pool, const int64_t* block_pairs, int64_t n_pairs,
                 int64_t num_blocks, int64_t block_bytes, void* stream);
@@ -199,7 +212,9 @@ PA_API int copy_blocks(void* k_pool, void* v_pool, const int64_t* block_pairs, i
  *                A dst must not appear twice (checked mode rejects it); out-of-range ids are
  *                skipped on the device and recorded as PA_DEVERR_COPY_PAIR.
  *   block_bytes  bytes of one block of one pool (block_size * n_kv_heads * head_dim * element size),
- *                a multiple of 16.  The copy is bit-exact and ordered on `stream`.
+ *                a multiple of 16.  With unified K/V blocks both sides use that layout: each
+ *                v pointer = its k pointer + block_bytes.  The copy is bit-exact and ordered on
+ *                `stream`.
  */
 PA_API int swap_blocks(void* dst_k_pool, void* dst_v_pool, int64_t dst_num_blocks, const void* src_k_pool,
                        const void* src_v_pool, int64_t src_num_blocks, const int64_t* block_pairs, int64_t n_pairs,

@@ -22,7 +22,8 @@ _DTYPE_CODES = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16, torch.float32: 
 
 PA_OK, PA_EINVAL, PA_EDTYPE, PA_ERANGE, PA_EWORKSPACE, PA_ECUDA, PA_EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 PA_OPT_CHECKED, PA_OPT_DECODE_KERNEL, PA_OPT_PARTITION_TOKENS, PA_OPT_PREFILL_KERNEL = 1, 2, 3, 4
-PA_OPT_CLUSTER_MERGE = 5
+PA_OPT_CLUSTER_MERGE, PA_OPT_KV_LAYOUT = 5, 6
+KV_LAYOUT_SEPARATE, KV_LAYOUT_UNIFIED = 0, 1
 PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT, PA_DEVERR_CONTEXT_LEN = 1, 2, 4
 PA_DEVERR_COPY_PAIR, PA_DEVERR_QUERY_LOC, PA_DEVERR_TIMEOUT = 8, 16, 32
 
@@ -122,6 +123,35 @@ def _pool_dims(k_pool: torch.Tensor, v_pool: torch.Tensor):
     return tuple(int(x) for x in k_pool.shape)
 
 
+def unified_views(pool: torch.Tensor):
+    """K and V views ``[num_blocks, block_size, n_kv_heads, head_dim]`` of a unified K/V pool
+    ``[num_blocks, 2, block_size, n_kv_heads, head_dim]`` (block b holds its keys, then its values).
+    Pass them as ``k_pool, v_pool`` while ``PA_OPT_KV_LAYOUT`` is ``KV_LAYOUT_UNIFIED``."""
+    if pool.dim() != 5 or pool.shape[1] != 2 or not pool.is_contiguous():
+        raise ValueError("a unified pool is a contiguous [num_blocks, 2, block_size, n_kv_heads, head_dim] tensor")
+    return pool[:, 0], pool[:, 1]
+
+
+def _pool(t: torch.Tensor, name: str, dtype=None, host_ok: bool = False) -> int:
+    """Pointer of a K or V pool after checking that its strides match the library's pool layout:
+    contiguous for separate pools, block stride doubled for the views of a unified pool."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [num_blocks, block_size, n_kv_heads, head_dim]")
+    _, S, Hkv, D = (int(x) for x in t.shape)
+    unified = get_option(PA_OPT_KV_LAYOUT) == KV_LAYOUT_UNIFIED
+    want = ((2 if unified else 1) * S * Hkv * D, Hkv * D, D, 1)
+    if tuple(t.stride()) != want:
+        layout = "a view of a unified K/V pool" if unified else "contiguous"
+        raise ValueError(f"{name} must be {layout} (strides {want}, got {tuple(t.stride())})")
+    return t.data_ptr()
+
+
 # ----------------------------------------------------------------------------------------------
 # entry points
 # ----------------------------------------------------------------------------------------------
@@ -135,8 +165,8 @@ def paged_kv_write(k_new, v_new, slot_mapping, k_pool, v_pool, stream=None):
         raise ValueError("k_new / v_new must be [T, n_kv_heads, head_dim] matching slot_mapping")
     dt = k_pool.dtype
     st = lib.paged_kv_write(_dev(k_new, "k_new", dt), _dev(v_new, "v_new", dt),
-                            _dev(slot_mapping, "slot_mapping", torch.int64), T, _dev(k_pool, "k_pool", dt),
-                            _dev(v_pool, "v_pool", dt), NB, S, Hkv, D, _code(dt), _stream(stream))
+                            _dev(slot_mapping, "slot_mapping", torch.int64), T, _pool(k_pool, "k_pool", dt),
+                            _pool(v_pool, "v_pool", dt), NB, S, Hkv, D, _code(dt), _stream(stream))
     _check("paged_kv_write", st)
 
 
@@ -188,8 +218,8 @@ def paged_attention_decode(q, k_pool, v_pool, block_table, context_lens, scale=N
         ws = workspace
     ws_ptr = _dev(ws, "workspace", torch.uint8) if ws is not None else None
     ws_bytes = int(ws.numel()) if ws is not None else 0
-    st = lib.paged_attention_decode(_dev(out, "out", dt), _dev(q, "q", dt), _dev(k_pool, "k_pool", dt),
-                                    _dev(v_pool, "v_pool", dt),
+    st = lib.paged_attention_decode(_dev(out, "out", dt), _dev(q, "q", dt), _pool(k_pool, "k_pool", dt),
+                                    _pool(v_pool, "v_pool", dt),
                                     _dev(block_table, "block_table", torch.int32, contiguous=False), bt_stride,
                                     _dev(context_lens, "context_lens", torch.int32), B, NB, S, float(scale),
                                     Hq, Hkv, D, _code(dt), ws_ptr, ws_bytes, _stream(stream))
@@ -222,7 +252,7 @@ def paged_attention_decode_fused(q, k_new, v_new, slot_mapping, k_pool, v_pool, 
     ws = _workspace(q.device, decode_workspace_size(B, bt_stride, S, Hq, Hkv, D)) if workspace == "auto" else workspace
     st = lib.paged_attention_decode_fused(
         _dev(out, "out", dt), _dev(q, "q", dt), _dev(k_new, "k_new", dt), _dev(v_new, "v_new", dt),
-        _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_pool, "k_pool", dt), _dev(v_pool, "v_pool", dt),
+        _dev(slot_mapping, "slot_mapping", torch.int64), _pool(k_pool, "k_pool", dt), _pool(v_pool, "v_pool", dt),
         _dev(block_table, "block_table", torch.int32, contiguous=False), bt_stride,
         _dev(context_lens, "context_lens", torch.int32), B, NB, S, float(scale), Hq, Hkv, D, _code(dt),
         _dev(ws, "workspace", torch.uint8) if ws is not None else None, int(ws.numel()) if ws is not None else 0,
@@ -255,7 +285,7 @@ def paged_attention_decode_static_scratch(q, k_pool, v_pool, block_table, contex
     if out is None:
         out = torch.empty_like(q)
     st = lib.paged_attention_decode_static_scratch(
-        _dev(out, "out", dt), _dev(q, "q", dt), _dev(k_pool, "k_pool", dt), _dev(v_pool, "v_pool", dt),
+        _dev(out, "out", dt), _dev(q, "q", dt), _pool(k_pool, "k_pool", dt), _pool(v_pool, "v_pool", dt),
         _dev(block_table, "block_table", torch.int32, contiguous=False), int(block_table.stride(0)),
         _dev(context_lens, "context_lens", torch.int32), B, NB, S, float(scale), Hq, Hkv, D, _code(dt),
         _stream(stream))
@@ -284,7 +314,7 @@ def paged_attention_prefill(q, query_start_loc, k_pool, v_pool, block_table, con
         raise ValueError("block_table rows must be contiguous")
     st = lib.paged_attention_prefill(_dev(out, "out", dt), _dev(q, "q", dt),
                                      _dev(query_start_loc, "query_start_loc", torch.int32), total_q,
-                                     _dev(k_pool, "k_pool", dt), _dev(v_pool, "v_pool", dt),
+                                     _pool(k_pool, "k_pool", dt), _pool(v_pool, "v_pool", dt),
                                      _dev(block_table, "block_table", torch.int32, contiguous=False),
                                      int(block_table.stride(0)), _dev(context_lens, "context_lens", torch.int32),
                                      B, NB, S, float(scale), Hq, Hkv, D, _code(dt), _stream(stream))
@@ -300,7 +330,7 @@ def copy_blocks(k_pool, v_pool, block_pairs, stream=None):
     if block_pairs.numel() and (block_pairs.dim() != 2 or block_pairs.shape[1] != 2):
         raise ValueError("block_pairs must be [n, 2]")
     block_bytes = S * Hkv * D * k_pool.element_size()
-    st = lib.copy_blocks(_dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+    st = lib.copy_blocks(_pool(k_pool, "k_pool"), _pool(v_pool, "v_pool"),
                          _dev(block_pairs, "block_pairs", torch.int64) if n else None, n, NB, block_bytes,
                          _stream(stream))
     _check("copy_blocks", st)
@@ -314,11 +344,12 @@ def swap_blocks(dst_k_pool, dst_v_pool, src_k_pool, src_v_pool, block_pairs, str
     if dst_k_pool.shape[1:] != src_k_pool.shape[1:] or dst_k_pool.dtype != src_k_pool.dtype:
         raise ValueError("source and destination pools must share block shape and dtype")
     for name, t in (("dst_k_pool", dst_k_pool), ("dst_v_pool", dst_v_pool), ("src_k_pool", src_k_pool),
-                    ("src_v_pool", src_v_pool), ("block_pairs", block_pairs)):
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
-        if not t.is_cuda and not t.is_pinned():
-            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+                    ("src_v_pool", src_v_pool)):
+        _pool(t, name, host_ok=True)
+    if not block_pairs.is_contiguous():
+        raise ValueError("block_pairs must be contiguous")
+    if not block_pairs.is_cuda and not block_pairs.is_pinned():
+        raise ValueError("block_pairs must be a CUDA tensor or pinned host memory")
     n = int(block_pairs.shape[0]) if block_pairs.numel() else 0
     if block_pairs.dtype != torch.int64 or (n and (block_pairs.dim() != 2 or block_pairs.shape[1] != 2)):
         raise ValueError("block_pairs must be int64 [n, 2]")

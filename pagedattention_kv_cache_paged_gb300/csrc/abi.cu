@@ -64,6 +64,19 @@ int log2i(int64_t x) {
 }
 bool checked() { return g_options[PA_OPT_CHECKED].load() != 0; }
 
+// Distance in bytes from one block of a pool to the next.  Separate pools: one block.  Unified K/V
+// blocks (one pool [num_blocks][2][block bytes]): two, and v_pool must be the V half of block 0,
+// i.e. k_pool + block_bytes.
+int pool_block_stride(const void* k_pool, const void* v_pool, int64_t block_bytes, int64_t* stride_bytes) {
+  if (g_options[PA_OPT_KV_LAYOUT].load() == 0) {
+    *stride_bytes = block_bytes;
+    return PA_OK;
+  }
+  if (static_cast<const char*>(v_pool) != static_cast<const char*>(k_pool) + block_bytes) return PA_EINVAL;
+  *stride_bytes = 2 * block_bytes;
+  return PA_OK;
+}
+
 int check_dtype(pa_dtype dt) { return (dt == PA_BF16 || dt == PA_FP16 || dt == PA_FP32) ? PA_OK : PA_EDTYPE; }
 
 int check_heads(int n_q_heads, int n_kv_heads, int head_dim) {
@@ -157,6 +170,7 @@ int pa_set_option(int option, int64_t value) {
       if (value < 0 || value > (int64_t(1) << 30)) return PA_EINVAL;
       break;
     case PA_OPT_CLUSTER_MERGE:
+    case PA_OPT_KV_LAYOUT:
       if (value != 0 && value != 1) return PA_EINVAL;
       break;
     default:
@@ -167,7 +181,7 @@ int pa_set_option(int option, int64_t value) {
 }
 
 int64_t pa_get_option(int option) {
-  if (option < 1 || option > 5) return PA_EINVAL;
+  if (option < 1 || option > 6) return PA_EINVAL;
   return g_options[option].load();
 }
 
@@ -214,6 +228,9 @@ int paged_kv_write(const void* k_new, const void* v_new, const int64_t* slot_map
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool)) return PA_EINVAL;
   const int64_t row_bytes = (int64_t)n_kv_heads * head_dim * dtype_bytes(dtype);
   if (row_bytes % 16 != 0) return PA_EUNSUPPORTED;
+  int64_t stride_bytes = 0;
+  rc = pool_block_stride(k_pool, v_pool, row_bytes * block_size, &stride_bytes);
+  if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned* err = nullptr;
   rc = device_info(&err, nullptr);
@@ -229,7 +246,8 @@ int paged_kv_write(const void* k_new, const void* v_new, const int64_t* slot_map
       if (v >= total_slots || !seen.insert(v).second) return PA_ERANGE;
     }
   }
-  KvWriteArgs a{k_new, v_new, slot_mapping, n_tokens, k_pool, v_pool, total_slots, (int)(row_bytes / 16), err};
+  KvWriteArgs a{k_new,        v_new,     slot_mapping,      n_tokens, k_pool, v_pool, total_slots,
+                (int)(row_bytes / 16), block_size, stride_bytes / 16, err};
   int launches = 0;
   cudaError_t e = launch_kv_write(a, dtype, s, &launches);
   return finish(e, launches);
@@ -260,6 +278,10 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PA_EINVAL;
   const bool fused = k_new != nullptr || v_new != nullptr || slot_mapping != nullptr;
   if (fused && (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new))) return PA_EINVAL;
+  const int64_t block_elems = (int64_t)block_size * n_kv_heads * head_dim;
+  int64_t stride_bytes = 0;
+  rc = pool_block_stride(k_pool, v_pool, block_elems * dtype_bytes(dtype), &stride_bytes);
+  if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned* err = nullptr;
   int sms = 0;
@@ -319,6 +341,7 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.block_shift = log2i(block_size);
+  a.kv_block_stride = stride_bytes / dtype_bytes(dtype);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.n_q_heads = n_q_heads;
   a.n_kv_heads = n_kv_heads;
@@ -397,6 +420,10 @@ int paged_attention_prefill(void* out, const void* q, const int32_t* query_start
   if (batch == 0 || total_q == 0) return PA_OK;
   if (!out || !q || !query_start_loc || !k_pool || !v_pool || !block_table || !context_lens) return PA_EINVAL;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PA_EINVAL;
+  int64_t stride_bytes = 0;
+  rc = pool_block_stride(k_pool, v_pool, (int64_t)block_size * n_kv_heads * head_dim * dtype_bytes(dtype),
+                         &stride_bytes);
+  if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned* err = nullptr;
   rc = device_info(&err, nullptr);
@@ -432,6 +459,7 @@ int paged_attention_prefill(void* out, const void* q, const int32_t* query_start
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.block_shift = log2i(block_size);
+  a.kv_block_stride = stride_bytes / dtype_bytes(dtype);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.n_q_heads = n_q_heads;
   a.n_kv_heads = n_kv_heads;
@@ -453,9 +481,12 @@ int copy_blocks(void* k_pool, void* v_pool, const int64_t* block_pairs, int64_t 
   if (n_pairs == 0) return PA_OK;
   if (!k_pool || !v_pool || !block_pairs) return PA_EINVAL;
   if (!aligned16(k_pool) || !aligned16(v_pool)) return PA_EINVAL;
+  int64_t stride_bytes = 0;
+  int rc = pool_block_stride(k_pool, v_pool, block_bytes, &stride_bytes);
+  if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned* err = nullptr;
-  int rc = device_info(&err, nullptr);
+  rc = device_info(&err, nullptr);
   if (rc) return rc;
   if (checked()) {
     std::vector<int64_t> pairs;
@@ -471,7 +502,7 @@ int copy_blocks(void* k_pool, void* v_pool, const int64_t* block_pairs, int64_t 
     for (int64_t d : dsts)
       if (srcs.count(d)) return PA_ERANGE;
   }
-  CopyBlocksArgs a{k_pool, v_pool, block_pairs, n_pairs, num_blocks, block_bytes / 16, err};
+  CopyBlocksArgs a{k_pool, v_pool, block_pairs, n_pairs, num_blocks, block_bytes / 16, stride_bytes / 16, err};
   int launches = 0;
   cudaError_t e = launch_copy_blocks(a, s, &launches);
   return finish(e, launches);
@@ -505,9 +536,14 @@ int swap_blocks(void* dst_k_pool, void* dst_v_pool, int64_t dst_num_blocks, cons
   if (!dst_k_pool || !dst_v_pool || !src_k_pool || !src_v_pool || !block_pairs) return PA_EINVAL;
   if (!aligned16(dst_k_pool) || !aligned16(dst_v_pool) || !aligned16(src_k_pool) || !aligned16(src_v_pool))
     return PA_EINVAL;
+  int64_t stride_bytes = 0, src_stride = 0;
+  int rc = pool_block_stride(dst_k_pool, dst_v_pool, block_bytes, &stride_bytes);
+  if (rc) return rc;
+  rc = pool_block_stride(src_k_pool, src_v_pool, block_bytes, &src_stride);
+  if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned* err = nullptr;
-  int rc = device_info(&err, nullptr);
+  rc = device_info(&err, nullptr);
   if (rc) return rc;
   SwapArgs a{};
   void* p = nullptr;
@@ -536,6 +572,7 @@ int swap_blocks(void* dst_k_pool, void* dst_v_pool, int64_t dst_num_blocks, cons
   a.src_num_blocks = src_num_blocks;
   a.dst_num_blocks = dst_num_blocks;
   a.block_vecs = block_bytes / 16;
+  a.block_stride_vecs = stride_bytes / 16;
   a.err = err;
   int launches = 0;
   cudaError_t e = launch_swap_blocks(a, s, &launches);

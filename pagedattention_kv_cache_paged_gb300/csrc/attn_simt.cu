@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(const AttnAr
   const int64_t row_elems = (int64_t)a.n_kv_heads * D;  // elements per pool slot
   // fused write (decode rows only): the partition holding the last context position writes this
   // step's K/V row there and takes it straight from k_new / v_new
-  int64_t new_row = -1, patch_pos = -1;
+  int64_t new_row = -1, patch_pos = -1;  // new_row: element offset of the new token's pool row
   if (a.k_new != nullptr && a.query_start_loc == nullptr && len > 0 && part == n_parts_row - 1) {
     const int64_t last = len - 1;
     const int64_t s_new = __ldg(a.slot_mapping + b);
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(const AttnAr
                                ? ((int64_t)blk_last << a.block_shift) + (last & (a.block_size - 1)) : -2;
     if (s_new >= 0) {
       if (s_new == expect) {
-        new_row = s_new;
+        new_row = (int64_t)blk_last * a.kv_block_stride + (last & (a.block_size - 1)) * row_elems;
         patch_pos = last;
       } else if (threadIdx.x == 0) {
         raise_error(a.err, PA_DEVERR_SLOT);
@@ -140,13 +140,13 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(const AttnAr
           const int64_t off = ((int64_t)b * a.n_kv_heads + kvh) * D + dsub * kVec;
           kr[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.k_new) + off));
           vr[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.v_new) + off));
-          const int64_t poff = new_row * row_elems + (int64_t)kvh * D + dsub * kVec;
+          const int64_t poff = new_row + (int64_t)kvh * D + dsub * kVec;
           *reinterpret_cast<uint4*>(static_cast<T*>(a.k_pool_w) + poff) = kr[u];
           *reinterpret_cast<uint4*>(static_cast<T*>(a.v_pool_w) + poff) = vr[u];
         } else {
-          const int64_t slot = ((int64_t)blk << a.block_shift) + (t & bmask);
-          kr[u] = ld_stream16(kbase + slot * row_elems);
-          vr[u] = ld_stream16(vbase + slot * row_elems);
+          const int64_t off = (int64_t)blk * a.kv_block_stride + (t & bmask) * row_elems;
+          kr[u] = ld_stream16(kbase + off);
+          vr[u] = ld_stream16(vbase + off);
         }
       }
     }

@@ -17,7 +17,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(uint4* __rest
                                                                    uint4* __restrict__ v_pool,
                                                                    const int64_t* __restrict__ pairs,
                                                                    int64_t num_blocks, int64_t block_vecs,
-                                                                   unsigned* err) {
+                                                                   int64_t block_stride_vecs, unsigned* err) {
   const int64_t p = blockIdx.x;
   const int64_t src = __ldg(pairs + 2 * p);
   const int64_t dst = __ldg(pairs + 2 * p + 1);
@@ -27,10 +27,10 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(uint4* __rest
   }
   const int64_t slice = (int64_t)kCopyThreads * kCopyUnroll;
   const int64_t base = (int64_t)blockIdx.y * slice + threadIdx.x;
-  const uint4* ks = k_pool + src * block_vecs;
-  const uint4* vs = v_pool + src * block_vecs;
-  uint4* kd = k_pool + dst * block_vecs;
-  uint4* vd = v_pool + dst * block_vecs;
+  const uint4* ks = k_pool + src * block_stride_vecs;
+  const uint4* vs = v_pool + src * block_stride_vecs;
+  uint4* kd = k_pool + dst * block_stride_vecs;
+  uint4* vd = v_pool + dst * block_stride_vecs;
   uint4 kb[kCopyUnroll], vb[kCopyUnroll];
 #pragma unroll
   for (int u = 0; u < kCopyUnroll; ++u) {
@@ -58,7 +58,7 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t s, int* lau
   dim3 grid((unsigned)a.n_pairs, (unsigned)ny);
   copy_blocks_kernel<<<grid, kCopyThreads, 0, s>>>(static_cast<uint4*>(a.k_pool),
                                                    static_cast<uint4*>(a.v_pool), a.pairs,
-                                                   a.num_blocks, a.block_vecs, a.err);
+                                                   a.num_blocks, a.block_vecs, a.block_stride_vecs, a.err);
   ++*launches;
   return cudaGetLastError();
 }
@@ -87,10 +87,10 @@ __global__ void __launch_bounds__(kSwapThreads) swap_blocks_kernel(const SwapArg
   }
   const int64_t slice = (int64_t)kSwapThreads * kSwapUnroll;
   const int64_t base = (int64_t)blockIdx.y * slice + threadIdx.x;
-  const uint4* ks = static_cast<const uint4*>(a.src_k) + src * a.block_vecs;
-  const uint4* vs = static_cast<const uint4*>(a.src_v) + src * a.block_vecs;
-  uint4* kd = static_cast<uint4*>(a.dst_k) + dst * a.block_vecs;
-  uint4* vd = static_cast<uint4*>(a.dst_v) + dst * a.block_vecs;
+  const uint4* ks = static_cast<const uint4*>(a.src_k) + src * a.block_stride_vecs;
+  const uint4* vs = static_cast<const uint4*>(a.src_v) + src * a.block_stride_vecs;
+  uint4* kd = static_cast<uint4*>(a.dst_k) + dst * a.block_stride_vecs;
+  uint4* vd = static_cast<uint4*>(a.dst_v) + dst * a.block_stride_vecs;
   uint4 kb[kSwapUnroll], vb[kSwapUnroll];
 #pragma unroll
   for (int u = 0; u < kSwapUnroll; ++u) {

@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   // fused write: the CTA holding the last context position writes this step's K/V row of its KV
   // head there and uses it straight from k_new / v_new (nanoserve Day 19, "What I added today":
   // write this step's K/V, then attend over the whole history)
-  int64_t new_row = -1;
+  int64_t new_row = -1;  // element offset of the new token's pool row
   if (a.k_new != nullptr && len > 0 && part == n_parts_row - 1) {
     const int64_t last = len - 1;
     const int64_t s_new = __ldg(a.slot_mapping + b);
@@ -121,8 +121,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
     const int64_t expect = (blk_last >= 0 && blk_last < a.num_blocks)
                                ? ((int64_t)blk_last << a.block_shift) + (last & bmask) : -2;
     if (s_new >= 0) {
-      if (s_new == expect) new_row = s_new;
-      else if (threadIdx.x == 0) raise_error(a.err, PA_DEVERR_SLOT);
+      if (s_new == expect)
+        new_row = (int64_t)blk_last * a.kv_block_stride + (last & bmask) * ((int64_t)a.n_kv_heads * D);
+      else if (threadIdx.x == 0)
+        raise_error(a.err, PA_DEVERR_SLOT);
     }
   }
   const int patch_tile = new_row >= 0 ? (int)((len - 1 - t_begin) / kTile) : -1;
@@ -151,14 +153,15 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
       mbar_arrive(&my_bars[s]);  // complete the phase without data; the consumer skips the tile
       return;
     }
-    const int y = (int)(((int64_t)blk << a.block_shift) + (tile_t0(j) & bmask));
+    const int off = (int)(tile_t0(j) & bmask);
     uint8_t* st = my_stages + s * kStageBytes;
     mbar_arrive_expect_tx(&my_bars[s], kStageBytes);
 #pragma unroll
-    for (int h = 0; h < kHalves; ++h) tma_load_2d(st + h * kHalfBytes, &kmap, kvh * D + h * 64, y, &my_bars[s]);
+    for (int h = 0; h < kHalves; ++h)
+      tma_load_3d(st + h * kHalfBytes, &kmap, kvh * D + h * 64, off, blk, &my_bars[s]);
 #pragma unroll
     for (int h = 0; h < kHalves; ++h)
-      tma_load_2d(st + (kHalves + h) * kHalfBytes, &vmap, kvh * D + h * 64, y, &my_bars[s]);
+      tma_load_3d(st + (kHalves + h) * kHalfBytes, &vmap, kvh * D + h * 64, off, blk, &my_bars[s]);
   };
   if (lane == 0) {
     const int pre = my_tiles < kStages ? my_tiles : kStages;
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
           const uint4 val = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(isv ? a.v_new : a.k_new) + src_off));
           *reinterpret_cast<uint4*>(st + ((isv ? kHalves : 0) + (c >> 3)) * kHalfBytes + r * 128 +
                                     (((c & 7) ^ (r & 7)) << 4)) = val;
-          T* dst = static_cast<T*>(isv ? a.v_pool_w : a.k_pool_w) + (new_row * a.n_kv_heads + kvh) * D + c * 8;
+          T* dst = static_cast<T*>(isv ? a.v_pool_w : a.k_pool_w) + new_row + (int64_t)kvh * D + c * 8;
           *reinterpret_cast<uint4*>(dst) = val;
         }
         __syncwarp();
@@ -410,17 +413,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// Pool viewed as [num_blocks * block_size][n_kv_heads * head_dim], boxes of 16 rows x 64 columns.
+// Pool viewed as a 3-D tensor (column in [0, n_kv_heads * head_dim), token in block, block) with the
+// pool's own block stride (so separate pools and unified K/V blocks share one code path); boxes of
+// 64 columns x 16 tokens x 1 block.
 bool encode_pool_map(CUtensorMap* map, const void* pool, pa_dtype dt, int64_t num_blocks, int block_size,
-                     int n_kv_heads, int head_dim) {
+                     int n_kv_heads, int head_dim, int64_t block_stride) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)n_kv_heads * head_dim, (cuuint64_t)num_blocks * block_size};
-  const cuuint64_t strides[1] = {(cuuint64_t)n_kv_heads * head_dim * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)kTile};
-  const cuuint32_t estr[2] = {1, 1};
+  const cuuint64_t dims[3] = {(cuuint64_t)n_kv_heads * head_dim, (cuuint64_t)block_size, (cuuint64_t)num_blocks};
+  const cuuint64_t strides[2] = {(cuuint64_t)n_kv_heads * head_dim * 2, (cuuint64_t)block_stride * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType ty = dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUresult r = fn(map, ty, 2, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  CUresult r = fn(map, ty, 3, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -430,7 +435,7 @@ bool decode_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, i
   if (block_size % kTile != 0) return false;
   if (head_dim != 64 && head_dim != 128) return false;
   if (group > 8) return false;
-  if (num_blocks * block_size >= (int64_t(1) << 31)) return false;  // TMA row coordinate is int32
+  if (num_blocks >= (int64_t(1) << 31)) return false;  // TMA block coordinate is int32
   return encode_fn() != nullptr;
 }
 
@@ -490,8 +495,8 @@ static cudaError_t launch_tc_t(const AttnArgs& a, const CUtensorMap& km, const C
 cudaError_t launch_decode_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches) {
   if (a.rows == 0) return cudaSuccess;
   CUtensorMap km, vm;
-  if (!encode_pool_map(&km, a.k_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim) ||
-      !encode_pool_map(&vm, a.v_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim))
+  if (!encode_pool_map(&km, a.k_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride) ||
+      !encode_pool_map(&vm, a.v_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride))
     return cudaErrorInvalidValue;
   cudaError_t e = dt == PA_BF16 ? launch_tc_t<__nv_bfloat16>(a, km, vm, s) : launch_tc_t<__half>(a, km, vm, s);
   ++*launches;

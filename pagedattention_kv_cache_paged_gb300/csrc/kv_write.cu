@@ -15,7 +15,8 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__
                                                        const int64_t* __restrict__ slots,
                                                        int64_t n_tokens, uint4* __restrict__ k_pool,
                                                        uint4* __restrict__ v_pool, int64_t total_slots,
-                                                       int row_vecs, unsigned* err) {
+                                                       int row_vecs, int block_size, int64_t block_stride_vecs,
+                                                       unsigned* err) {
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t total = n_tokens * row_vecs;
   if (idx >= total) return;
@@ -29,8 +30,10 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__
   }
   const uint4 kv = __ldg(k_new + idx);
   const uint4 vv = __ldg(v_new + idx);
-  k_pool[slot * row_vecs + c] = kv;
-  v_pool[slot * row_vecs + c] = vv;
+  const int64_t blk = slot / block_size;
+  const int64_t row = blk * block_stride_vecs + (slot - blk * block_size) * row_vecs;
+  k_pool[row + c] = kv;
+  v_pool[row + c] = vv;
 }
 
 cudaError_t launch_kv_write(const KvWriteArgs& a, pa_dtype, cudaStream_t s, int* launches) {
@@ -41,7 +44,7 @@ cudaError_t launch_kv_write(const KvWriteArgs& a, pa_dtype, cudaStream_t s, int*
   kv_write_kernel<<<(unsigned)blocks, threads, 0, s>>>(
       static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new), a.slot_mapping,
       a.n_tokens, static_cast<uint4*>(a.k_pool), static_cast<uint4*>(a.v_pool), a.total_slots,
-      a.row_vecs, a.err);
+      a.row_vecs, a.block_size, a.block_stride_vecs, a.err);
   ++*launches;
   return cudaGetLastError();
 }

@@ -2,6 +2,7 @@
 // Host-only declarations; no torch types, no device code.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,6 +22,8 @@ struct KvWriteArgs {
   void* v_pool;
   int64_t total_slots;   // num_blocks * block_size
   int row_vecs;          // n_kv_heads * head_dim * elt / 16 (16-byte vectors per token row)
+  int block_size;
+  int64_t block_stride_vecs;  // 16-byte vectors from one block of a pool to the next
   unsigned* err;         // device error word
 };
 
@@ -31,6 +34,7 @@ struct CopyBlocksArgs {
   int64_t n_pairs;
   int64_t num_blocks;
   int64_t block_vecs;    // block_bytes / 16
+  int64_t block_stride_vecs;  // 16-byte vectors from one block of a pool to the next
   unsigned* err;
 };
 
@@ -45,6 +49,7 @@ struct SwapArgs {
   int64_t src_num_blocks;
   int64_t dst_num_blocks;
   int64_t block_vecs;    // block_bytes / 16
+  int64_t block_stride_vecs;  // 16-byte vectors from one block of a pool to the next (both pools)
   unsigned* err;
 };
 
@@ -63,6 +68,8 @@ struct AttnArgs {
   int64_t num_blocks;
   int block_size;
   int block_shift;                 // log2(block_size)
+  int64_t kv_block_stride;         // elements from one block of a pool to the next (separate pools:
+                                   // block_size * n_kv_heads * head_dim; unified K/V blocks: twice that)
   float scale_log2;                // scale * log2(e)
   int n_q_heads;
   int n_kv_heads;
@@ -111,6 +118,11 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t s, int* lau
 cudaError_t launch_swap_blocks(const SwapArgs& a, cudaStream_t s, int* launches);
 cudaError_t launch_attn_simt(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
 cudaError_t launch_lse_merge(const MergeArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
+
+// TMA view of a pool: 3-D tensor (column = n_kv_heads * head_dim, token in block, block) with the
+// pool's block stride, boxes of 64 columns x 16 tokens x 1 block, 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, const void* pool, pa_dtype dt, int64_t num_blocks, int block_size,
+                     int n_kv_heads, int head_dim, int64_t block_stride);
 
 // Tensor-core decode (TMA + mma.sync) for bf16/fp16 pools with block_size % 16 == 0.
 bool decode_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks);

@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             break;
           }
           uint32_t bytes = 0;
-          int ys[kSub];
+          int ys[kSub], yo[kSub];
 #pragma unroll
           for (int sub = 0; sub < kSub; ++sub) {
             const int64_t k0 = (int64_t)tile * kKeyTile + sub * 16;
@@ -155,7 +155,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               if (blk < 0 || blk >= a.num_blocks) {
                 raise_error(a.err, PA_DEVERR_BLOCK_ID);
               } else {
-                ys[sub] = (int)(((int64_t)blk << a.block_shift) + (k0 & bmask));
+                ys[sub] = blk;
+                yo[sub] = (int)(k0 & bmask);
                 bytes += 2 * kHalves * kBoxBytes;
               }
             }
@@ -171,8 +172,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
               for (int h = 0; h < kHalves; ++h) {
                 const int off = (sub * kHalves + h) * kBoxBytes;
-                tma_load_2d(st + off, &kmap, kvh * D + h * 64, ys[sub], &full[s]);
-                tma_load_2d(st + kOpBytes + off, &vmap, kvh * D + h * 64, ys[sub], &full[s]);
+                tma_load_3d(st + off, &kmap, kvh * D + h * 64, yo[sub], ys[sub], &full[s]);
+                tma_load_3d(st + kOpBytes + off, &vmap, kvh * D + h * 64, yo[sub], ys[sub], &full[s]);
               }
             }
           }
@@ -379,8 +380,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------------------
-bool encode_pool_map(CUtensorMap* map, const void* pool, pa_dtype dt, int64_t num_blocks, int block_size,
-                     int n_kv_heads, int head_dim);
 
 bool prefill_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks) {
   return decode_tc_supported(dt, block_size, head_dim, group, num_blocks);
@@ -425,8 +424,8 @@ static cudaError_t launch_pf_t(const AttnArgs& a, const CUtensorMap& km, const C
 cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches) {
   if (a.rows == 0) return cudaSuccess;
   CUtensorMap km, vm;
-  if (!encode_pool_map(&km, a.k_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim) ||
-      !encode_pool_map(&vm, a.v_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim))
+  if (!encode_pool_map(&km, a.k_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride) ||
+      !encode_pool_map(&vm, a.v_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride))
     return cudaErrorInvalidValue;
   cudaError_t e = dt == PA_BF16 ? launch_pf_t<__nv_bfloat16>(a, km, vm, s) : launch_pf_t<__half>(a, km, vm, s);
   ++*launches;

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
             alive = false;
             break;
           }
-          int ys[kUmSub];
+          int ys[kUmSub], yo[kUmSub];
           uint32_t bytes = 0;
 #pragma unroll
           for (int sub = 0; sub < kUmSub; ++sub) {
@@ -187,7 +187,8 @@ __global__ void __launch_bounds__(kUmThreads, 1)
               if (blk < 0 || blk >= a.num_blocks) {
                 if (!is_v) raise_error(a.err, PA_DEVERR_BLOCK_ID);
               } else {
-                ys[sub] = (int)(((int64_t)blk << a.block_shift) + (k0 & bmask));
+                ys[sub] = blk;
+                yo[sub] = (int)(k0 & bmask);
                 bytes += kHalves * 2048;
               }
             }
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
               if (ys[sub] < 0) continue;
 #pragma unroll
               for (int h = 0; h < kHalves; ++h)
-                tma_load_2d(st + h * Cfg::kKvHalf + sub * 2048, map, kvh * D + h * 64, ys[sub], &full[s]);
+                tma_load_3d(st + h * Cfg::kKvHalf + sub * 2048, map, kvh * D + h * 64, yo[sub], ys[sub], &full[s]);
             }
           }
         }
@@ -487,8 +488,6 @@ __global__ void __launch_bounds__(kUmThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------------------
-bool encode_pool_map(CUtensorMap* map, const void* pool, pa_dtype dt, int64_t num_blocks, int block_size,
-                     int n_kv_heads, int head_dim);
 
 template <typename T, int D, int G>
 static cudaError_t launch_um_g(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
@@ -524,8 +523,8 @@ static cudaError_t launch_um_d(const AttnArgs& a, const CUtensorMap& km, const C
 cudaError_t launch_prefill_umma(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches) {
   if (a.rows == 0) return cudaSuccess;
   CUtensorMap km, vm;
-  if (!encode_pool_map(&km, a.k_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim) ||
-      !encode_pool_map(&vm, a.v_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim))
+  if (!encode_pool_map(&km, a.k_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride) ||
+      !encode_pool_map(&vm, a.v_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride))
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (dt == PA_BF16)

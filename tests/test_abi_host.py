@@ -53,6 +53,26 @@ def test_options_validate(lib):
     assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 0) == 0
     assert lib.pa_set_option(pa.PA_OPT_CLUSTER_MERGE, 2) == pa.PA_EINVAL
     assert lib.pa_get_option(pa.PA_OPT_CLUSTER_MERGE) == 0
+    assert lib.pa_set_option(pa.PA_OPT_KV_LAYOUT, 2) == pa.PA_EINVAL
+    assert lib.pa_get_option(pa.PA_OPT_KV_LAYOUT) == pa.KV_LAYOUT_SEPARATE
+
+
+def test_unified_layout_requires_v_to_be_the_v_half_of_block_0(lib):
+    """With unified K/V blocks the V view must start one K half after the K view; any other pair
+    of pointers is refused before anything is launched (the pointers are never dereferenced)."""
+    half = 16 * 2 * 64 * 2
+    k = 1 << 20
+    assert lib.pa_set_option(pa.PA_OPT_KV_LAYOUT, pa.KV_LAYOUT_UNIFIED) == 0
+    try:
+        assert lib.copy_blocks(k, k + 2 * half, 1 << 24, 1, 4, half, None) == pa.PA_EINVAL
+        assert lib.copy_blocks(k + half, k, 1 << 24, 1, 4, half, None) == pa.PA_EINVAL
+        assert lib.paged_kv_write(1 << 24, 1 << 24, 1 << 24, 1, k, k + 16, 4, 16, 2, 64, pa.PA_BF16, None) \
+            == pa.PA_EINVAL
+        args = [1 << 24, 1 << 24, k, k + half // 2, 1 << 24, 4, 1 << 24, 2, 8, 16, 1.0]
+        assert lib.paged_attention_decode(*args, 8, 2, 64, pa.PA_BF16, None, 0, None) == pa.PA_EINVAL
+        assert lib.swap_blocks(k, k + half, 4, k, k + 3 * half, 4, 1 << 24, 1, half, None) == pa.PA_EINVAL
+    finally:
+        assert lib.pa_set_option(pa.PA_OPT_KV_LAYOUT, pa.KV_LAYOUT_SEPARATE) == 0
 
 
 def test_argument_errors_are_returned_before_any_launch(lib):
