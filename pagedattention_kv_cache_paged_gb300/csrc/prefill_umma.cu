@@ -11,16 +11,19 @@
 //   warps 0-3 / 4-7  softmax groups 0 / 1: thread t of group k owns row 128k + t (TMEM lane t of
 //              S_k and O_k); stages its Q row, turns each S_k tile into probabilities, rescales O_k
 //              in TMEM only when its stabilising maximum has to move up by more than 2^8, writes
-//              P_k (bf16/fp16) to shared memory, and normalises O_k at the end;
-//   warp 8     producer: lane 0 streams 64-key K tiles, lane 1 the matching V tiles (TMA boxes of
-//              16 keys x 64 columns from the physical blocks the table names) into a 3-stage K
-//              ring and a 2-stage V ring;
-//   warp 9     MMA: allocates TMEM (S_0, S_1: 64 columns each; O_0, O_1: head_dim each) and
-//              issues S_k = Q_k K^T (M 128, N 64) and O_k += P_k V (M 128, N head_dim, V as an
-//              MN-major operand) with tcgen05.mma, ordered so that the tensor core works on one
-//              group's products while the other group computes its softmax; each group releases its S
-//              as soon as it has been read out of TMEM, so the next S is computed during its
-//              exponentials.
+//              P_k (bf16/fp16) back into the TMEM columns of S_k, and normalises O_k at the end;
+//   warp 8     producer: lane 0 streams 128-key K tiles, lane 1 the matching V tiles (TMA boxes
+//              of 16 keys x 64 columns from the physical blocks the table names) into 2-stage
+//              rings;
+//   warp 9     MMA: allocates TMEM (S_0, S_1: 128 columns each; O_0, O_1: 128 columns each) and
+//              issues S_k = Q_k K^T (M 128, N 128, both operands in shared memory) and
+//              O_k += P_k V (M 128, N head_dim, P read from TMEM, V an MN-major shared-memory
+//              operand) with tcgen05.mma as soon as each product's inputs are ready, so that the
+//              tensor core works on one group's products while the other group computes its
+//              softmax.  S_k of the next tile is issued only after O_k += P_k V of this one has
+//              completed, because P_k lives in the columns the next S_k overwrites; that same
+//              ordering makes O_k stable whenever a group sees a new S_k, so rescaling needs no
+//              extra wait.
 // Every mbarrier wait is bounded (PA_DEVERR_TIMEOUT, with a cooperative abort); TMEM is always
 // released.  The stabilising maximum is exact bookkeeping: numerator and denominator use the
 // same one, so the result equals the running-max form of "Online Softmax" in real arithmetic.
@@ -35,11 +38,11 @@ namespace pa {
 constexpr int kUmThreads = 320;
 constexpr int kUmTileRows = 128;            // rows per Q tile (MMA M)
 constexpr int kUmRows = 2 * kUmTileRows;    // rows per CTA
-constexpr int kUmKeys = 64;                 // keys per K/V tile (N of S, K of PV)
+constexpr int kUmKeys = 128;                // keys per K/V tile (N of S, K of PV)
 constexpr int kUmSub = kUmKeys / 16;
 constexpr int kUmTmemCols = 512;
-constexpr int kUmKStages = 3;               // K ring depth
-constexpr int kUmVStages = 3;               // V ring depth
+constexpr int kUmKStages = 2;               // K ring depth
+constexpr int kUmVStages = 2;               // V ring depth
 constexpr float kUmRescaleThreshold = 8.f;  // log2 units: O is rescaled when the max grows by > 2^8
 
 template <int D>
@@ -49,13 +52,72 @@ struct UmCfg {
   static constexpr int kQBytes = kUmTileRows * D * 2;
   static constexpr int kKvHalf = kUmKeys * 128;      // one 64-column half of a K or V tile
   static constexpr int kKvBytes = kUmKeys * D * 2;
-  static constexpr int kPBytes = kUmTileRows * kUmKeys * 2;
-  static constexpr int kSmemBytes = 1024 + 1024 + 2 * kQBytes + (kUmKStages + kUmVStages) * kKvBytes + 4 * kPBytes;
+  static constexpr int kSmemBytes = 1024 + 1024 + 2 * kQBytes + (kUmKStages + kUmVStages) * kKvBytes;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
 // Byte offset of (row r, 8-element chunk c) in a [half][rows][128 B] swizzled operand.
 __device__ __forceinline__ uint32_t sw_off(int r, int c, int half_bytes) {
   return (uint32_t)((c >> 3) * half_bytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// Softmax helpers: one thread owns one row of S (its TMEM lane); `taddr` is the row's first column.
+// Keys whose bit is clear in mask[q] (chunk q = columns 32q .. 32q + 31) are outside the causal
+// bound or were not loaded; kMasked = false is the common case of a tile with every key valid.
+
+// Row maximum of the scaled scores.
+template <bool kMasked>
+__device__ __forceinline__ float s_row_max(uint32_t taddr, float sc, const uint32_t (&mask)[kUmKeys / 32]) {
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int q = 0; q < kUmKeys / 32; ++q) {
+    uint32_t v[32];
+    tmem_ld32(taddr + 32u * q, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      float x = __uint_as_float(v[j]) * sc;
+      if (kMasked) x = (mask[q] & (1u << j)) ? x : -INFINITY;
+      m[j & 3] = fmaxf(m[j & 3], x);
+    }
+  }
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// Probabilities 2^(sc * s - m_sub) (0 for masked keys), written back as 16-bit pairs into the first
+// kUmKeys / 2 columns of the row (keys 2c and 2c + 1 in column c); returns their sum.  Columns
+// [32 h, 32 h + 32) of P hold keys [64 h, 64 h + 64), which are read before they are overwritten.
+template <bool kMasked, bool kBf16>
+__device__ __forceinline__ float p_row_store(uint32_t taddr, float sc, float m_sub,
+                                             const uint32_t (&mask)[kUmKeys / 32]) {
+  static_assert(kUmKeys == 128, "two halves of 64 keys");
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1  // one half at a time keeps the register footprint at one chunk in, one chunk out
+  for (int h = 0; h < 2; ++h) {
+    uint32_t w[32];
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      const int q = 2 * h + q2;
+      const uint32_t mq = h == 0 ? mask[q2] : mask[2 + q2];
+      uint32_t v[32];
+      tmem_ld32(taddr + 32u * q, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        float e0 = fast_exp2(fmaf(__uint_as_float(v[j]), sc, -m_sub));
+        float e1 = fast_exp2(fmaf(__uint_as_float(v[j + 1]), sc, -m_sub));
+        if (kMasked) {
+          e0 = (mq & (1u << j)) ? e0 : 0.f;
+          e1 = (mq & (2u << j)) ? e1 : 0.f;
+        }
+        acc[j & 3] += e0;
+        acc[(j + 1) & 3] += e1;
+        w[16 * q2 + j / 2] = pack2<kBf16>(e0, e1);
+      }
+    }
+    tmem_st32(taddr + 32u * h, w);
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 template <typename T, int D, int G>
@@ -70,24 +132,22 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base);
-  uint64_t* kfull = bars + 0;     // [3]
-  uint64_t* kempty = bars + 3;    // [3] completes when both groups' S products have read the tile
-  uint64_t* vfull = bars + 6;     // [3]
-  uint64_t* vempty = bars + 9;    // [3] completes when both groups' P V products have read the tile
-  uint64_t* q_ready = bars + 12;
-  // per group k and buffer b (tile j uses buffer j % 2): [2 * k + b]
-  uint64_t* s_full = bars + 13;   // S_k^b computed
-  uint64_t* s_free = bars + 17;   // S_k^b read out of TMEM
-  uint64_t* p_full = bars + 21;   // P_k^b written (and O_k rescaled)
-  uint64_t* pv_done = bars + 25;  // O_k += P_k^b V finished
-  uint64_t* fin = bars + 29;
-  uint64_t* mready = bars + 30;   // [8] per tile slot: the sub-tile mask below is written
+  uint64_t* kfull = bars + 0;     // [kUmKStages]
+  uint64_t* kempty = bars + 4;    // [kUmKStages] completes when both groups' S products have read the tile
+  uint64_t* vfull = bars + 8;     // [kUmVStages]
+  uint64_t* vempty = bars + 12;   // [kUmVStages] completes when both groups' P V products have read the tile
+  uint64_t* q_ready = bars + 16;
+  // per group k, one phase per tile
+  uint64_t* s_full = bars + 17;   // [2] S_k computed (and, with it, every earlier product of the CTA)
+  uint64_t* p_full = bars + 19;   // [2] P_k written to TMEM (and O_k rescaled)
+  uint64_t* pv_done = bars + 21;  // [2] O_k += P_k V finished
+  uint64_t* fin = bars + 23;
+  uint64_t* mready = bars + 24;   // [8] per tile slot: the sub-tile mask below is written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 512);
   uint32_t* kmask = reinterpret_cast<uint32_t*>(base + 768);  // [8] sub-tiles holding data, per tile slot
   uint8_t* qs = base + 1024;                       // [2][Q tile]
   uint8_t* ks = qs + 2 * Cfg::kQBytes;             // [3 stages][K tile]
   uint8_t* vs = ks + kUmKStages * Cfg::kKvBytes;   // [2 stages][V tile]
-  uint8_t* ps = vs + kUmVStages * Cfg::kKvBytes;   // [2 groups][2 buffers][P tile]
 
   const int kvh = blockIdx.x % a.n_kv_heads;
   const int64_t T0 = (int64_t)(blockIdx.x / a.n_kv_heads) * kQB;
@@ -108,11 +168,10 @@ __global__ void __launch_bounds__(kUmThreads, 1)
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 2);
     }
-    for (int s = 0; s < 4; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 128);
-      mbar_init(&p_full[s], 128);
-      mbar_init(&pv_done[s], 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&s_full[k], 1);
+      mbar_init(&p_full[k], 128);
+      mbar_init(&pv_done[k], 1);
     }
     mbar_init(q_ready, 256);
     mbar_init(fin, 1);
@@ -125,8 +184,9 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // S_k^b at columns [64 (2k + b), +64), O_k at [256 + 128k, +D)
-  auto tS = [&](int k, int b) { return tmem + 64u * (uint32_t)(2 * k + b); };
+  // S_k at columns [128k, +128) (P_k, two 16-bit values per column, in its first 64), O_k at
+  // [256 + 128k, +D)
+  auto tS = [&](int k) { return tmem + 128u * (uint32_t)k; };
   auto tO = [&](int k) { return tmem + 256u + 128u * (uint32_t)k; };
 
   struct Seg {
@@ -195,8 +255,9 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           }
           if (!is_v) {
             // publish which sub-tiles hold data; the softmax groups read it instead of the table.
-            // Slot i % 8 was last read for tile i - 8, which both groups finished long ago: this
-            // lane cannot run more than 4 tiles ahead of them (K ring depth + one S in flight).
+            // Slot i % 8 was last read for tile i - 8, which both groups finished long ago: K tile
+            // i is loaded only after both S products of tile i - 2 completed, which needed each
+            // group's P of tile i - 3.
             unsigned m = 0;
 #pragma unroll
             for (int sub = 0; sub < kUmSub; ++sub) m |= (ys[sub] >= 0 ? 1u : 0u) << sub;
@@ -238,21 +299,21 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t qo = (kk >> 2) * Cfg::kQHalf + (kk & 3) * 32;
           const uint32_t ko = (kk >> 2) * Cfg::kKvHalf + (kk & 3) * 32;
-          umma_ss(tS(k, i & 1), umma_desc_sw128(qa + qo, 16, 1024), umma_desc_sw128(ka + ko, 16, 1024), id_s,
+          umma_ss(tS(k), umma_desc_sw128(qa + qo, 16, 1024), umma_desc_sw128(ka + ko, 16, 1024), id_s,
                   kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[2 * k + (i & 1)]);
+        umma_commit(&s_full[k]);
       };
       auto issue_pv = [&](int k, int i) {
-        const uint32_t pa_ = smem_u32(ps + (2 * k + (i & 1)) * Cfg::kPBytes);
         const uint32_t va = smem_u32(vs + (i % kUmVStages) * Cfg::kKvBytes);
+        // A = P_k from TMEM: 16 keys = 8 columns per instruction
 #pragma unroll
         for (int kk = 0; kk < kUmKeys / 16; ++kk)
-          umma_ss(tO(k), umma_desc_sw128(pa_ + kk * 32, 16, 1024),
-                  umma_desc_sw128(va + kk * 2048, Cfg::kKvHalf, 1024), id_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&pv_done[2 * k + (i & 1)]);
+          umma_ts(tO(k), tS(k) + 8u * (uint32_t)kk, umma_desc_sw128(va + kk * 2048, Cfg::kKvHalf, 1024), id_pv,
+                  (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&pv_done[k]);
       };
-      // Event-driven issue: each group's next S (needs its previous S read out and the K tile) and
+      // Event-driven issue: each group's next S (needs the K tile and its previous P V finished) and
       // next P V (needs its P and the V tile) are issued as soon as they are ready, so a slow group
       // never holds back the other group's products.
       bool alive = mbar_wait(q_ready, 0, a.err);
@@ -262,9 +323,9 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         bool progress = false;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          // S_k(j) overwrites buffer j % 2, last holding S_k(j - 2)
+          // S_k(j) overwrites P_k(j - 1): O_k += P_k(j - 1) V must have completed
           const int j = next_s[k];
-          if (j < n_all && (j < 2 || mbar_test(&s_free[2 * k + (j & 1)], (unsigned)(((j >> 1) - 1) & 1))) &&
+          if (j < n_all && j == next_pv[k] && (j == 0 || mbar_test(&pv_done[k], (unsigned)((j - 1) & 1))) &&
               mbar_test(&kfull[j % kUmKStages], (unsigned)((j / kUmKStages) & 1))) {
             tc_fence_after();
             issue_s(k, j);
@@ -275,8 +336,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           const int jp = next_pv[k];
           // group 1's P V follows group 0's for the same tile: group 0 zeroes the tile's stale V
           // rows before it signals p_full, and group 1 must not read them earlier
-          if (jp < next_s[k] && (k == 0 || next_pv[0] > jp) &&
-              mbar_test(&p_full[2 * k + (jp & 1)], (unsigned)((jp >> 1) & 1)) &&
+          if (jp < next_s[k] && (k == 0 || next_pv[0] > jp) && mbar_test(&p_full[k], (unsigned)(jp & 1)) &&
               mbar_test(&vfull[jp % kUmVStages], (unsigned)((jp / kUmVStages) & 1))) {
             tc_fence_after();
             issue_pv(k, jp);
@@ -333,46 +393,32 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           break;
         }
         const unsigned loaded = kmask[i & 7];
-        const int bsel = i & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[2 * grp + bsel], (unsigned)((i >> 1) & 1), a.err))) {
+        // S_k of this tile is complete, and with it O_k += P_k V of the previous tile (issued before)
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], (unsigned)(i & 1), a.err))) {
           alive = false;
           break;
         }
         tc_fence_after();
-        float x[kUmKeys];
-#pragma unroll
-        for (int c0 = 0; c0 < kUmKeys; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tS(grp, bsel) + lane_base + c0, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) x[c0 + j] = __uint_as_float(v[j]);
-        }
-        tc_fence_before();
-        mbar_arrive(&s_free[2 * grp + bsel]);  // this S buffer may now take tile i + 2
-        // a tile wholly inside this row's causal bound with every sub-tile loaded needs no mask
+        // tiles wholly inside every row's causal bound of the warp, with every sub-tile loaded, need
+        // no mask (the common case); the others mask per 32-key chunk
         const float sc = a.scale_log2;
-        const bool fast = sc > 0.f && loaded == (1u << kUmSub) - 1u && kb + kUmKeys - 1 <= bound;
-        float mx = -INFINITY;
-        if (fast) {
-#pragma unroll
-          for (int c = 0; c < kUmKeys; ++c) mx = fmaxf(mx, x[c]);
-          mx *= sc;
-        } else {
-          // bit c of `keep`: key kb + c is loaded and inside the causal bound
-          uint64_t keep = 0;
-#pragma unroll
-          for (int sub = 0; sub < kUmSub; ++sub)
-            if ((loaded >> sub) & 1u) keep |= 0xFFFFull << (16 * sub);
+        const unsigned all_sub = (1u << kUmSub) - 1u;
+        const bool unmasked = __all_sync(0xffffffffu, loaded == all_sub && kb + kUmKeys - 1 <= bound);
+        uint32_t mask[kUmKeys / 32];
+        {
           const int64_t lim = bound - kb;  // keys c <= lim are causal
-          if (lim < 0) keep = 0;
-          else if (lim < kUmKeys - 1) keep &= (2ull << lim) - 1ull;
+          const int nv = lim < 0 ? 0 : (lim >= kUmKeys ? kUmKeys : (int)lim + 1);
 #pragma unroll
-          for (int c = 0; c < kUmKeys; ++c) {
-            x[c] = ((keep >> c) & 1ull) ? x[c] * sc : -INFINITY;
-            mx = fmaxf(mx, x[c]);
+          for (int q = 0; q < kUmKeys / 32; ++q) {
+            const int lo = 32 * q;
+            const uint32_t cm = nv >= lo + 32 ? 0xFFFFFFFFu : (nv <= lo ? 0u : ((1u << (nv - lo)) - 1u));
+            const uint32_t lm = (((loaded >> (2 * q)) & 1u) ? 0x0000FFFFu : 0u) |
+                                (((loaded >> (2 * q + 1)) & 1u) ? 0xFFFF0000u : 0u);
+            mask[q] = cm & lm;
           }
         }
+        const uint32_t srow = tS(grp) + lane_base;
+        const float mx = unmasked ? s_row_max<false>(srow, sc, mask) : s_row_max<true>(srow, sc, mask);
         // move the stabiliser only when it must: first finite maximum, or growth beyond 2^8
         float corr = 1.f;
         if (mx > m_use + kUmRescaleThreshold || (m_use == -INFINITY && mx != -INFINITY)) {
@@ -380,33 +426,11 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           m_use = mx;
         }
         const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-        float rs = 0.f;
-        if (fast) {
-#pragma unroll
-          for (int c = 0; c < kUmKeys; ++c) {
-            x[c] = fast_exp2(fmaf(x[c], sc, -m_sub));
-            rs += x[c];
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kUmKeys; ++c) {
-            x[c] = fast_exp2(x[c] - m_sub);
-            rs += x[c];
-          }
-        }
+        const float rs = unmasked ? p_row_store<false, kBf16>(srow, sc, m_sub, mask)
+                                  : p_row_store<true, kBf16>(srow, sc, m_sub, mask);
         l_run = l_run * corr + rs;
-        // the P buffer of tile i - 2 must have been consumed, and O must be stable before a rescale
-        if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[2 * grp + bsel], (unsigned)(((i >> 1) - 1) & 1), a.err))) {
-          alive = false;
-          break;
-        }
+        // O_k is stable here (its last product completed before this S_k was issued)
         if (i > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-          const int pb = (i - 1) & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[2 * grp + pb], (unsigned)(((i - 1) >> 1) & 1), a.err))) {
-            alive = false;
-            break;
-          }
-          tc_fence_after();
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t v[32];
@@ -416,11 +440,10 @@ __global__ void __launch_bounds__(kUmThreads, 1)
             for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * corr);
             tmem_st32(tO(grp) + lane_base + c0, v);
           }
-          tmem_wait_st();
         }
         // group 0 zeroes V rows that hold no data or lie past the context (group 1's P V is issued
         // after group 0's, so it sees the zeros too)
-        if (grp == 0 && (kb + kUmKeys > sg.n || loaded != (1u << kUmSub) - 1u)) {
+        if (grp == 0 && (kb + kUmKeys > sg.n || loaded != all_sub)) {
           if (!__all_sync(0xffffffffu, mbar_wait(&vfull[i % kUmVStages], (unsigned)((i / kUmVStages) & 1), a.err))) {
             alive = false;
             break;
@@ -432,26 +455,17 @@ __global__ void __launch_bounds__(kUmThreads, 1)
             if (kb + key >= sg.n || !((loaded >> (key >> 4)) & 1u))
               *reinterpret_cast<uint4*>(vst + sw_off(key, c, Cfg::kKvHalf)) = make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async_smem();
         }
-        // P row into shared memory: [row][64 keys] = one 128-byte swizzled row
-#pragma unroll
-        for (int c = 0; c < kUmKeys / 8; ++c) {
-          uint4 w;
-          w.x = pack2<kBf16>(x[8 * c + 0], x[8 * c + 1]);
-          w.y = pack2<kBf16>(x[8 * c + 2], x[8 * c + 3]);
-          w.z = pack2<kBf16>(x[8 * c + 4], x[8 * c + 5]);
-          w.w = pack2<kBf16>(x[8 * c + 6], x[8 * c + 7]);
-          *reinterpret_cast<uint4*>(ps + (2 * grp + bsel) * Cfg::kPBytes + sw_off(r, c, kUmTileRows * 128)) = w;
-        }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full[2 * grp + bsel]);
+        mbar_arrive(&p_full[grp]);
       }
       t = sg.seg1;
     }
     if (!alive && lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
     if (alive && i > 0) {
-      alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[2 * grp + ((i - 1) & 1)], (unsigned)(((i - 1) >> 1) & 1), a.err));
+      alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[grp], (unsigned)((i - 1) & 1), a.err));
       tc_fence_after();
     }
     const bool have = alive && i > 0 && l_run != 0.f;
