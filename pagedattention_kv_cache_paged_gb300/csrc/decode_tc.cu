@@ -430,6 +430,23 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, pa_dtype dt, int64_t nu
   return r == CUDA_SUCCESS;
 }
 
+// Queries [total_q][n_q_heads][head_dim] viewed as a 3-D tensor (column, head, token); boxes of 64
+// columns x heads_box heads x tokens_box tokens with the 128-byte swizzle, so that one box lands as
+// heads_box * tokens_box rows of 128 bytes ordered (token, head).  Rows past total_q read as zeros.
+bool encode_q_map(CUtensorMap* map, const void* q, pa_dtype dt, int64_t total_q, int n_q_heads, int head_dim,
+                  int heads_box, int tokens_box) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_q_heads, (cuuint64_t)total_q};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_q_heads * head_dim * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)heads_box, (cuuint32_t)tokens_box};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType ty = dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(map, ty, 3, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool decode_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks) {
   if (dt != PA_BF16 && dt != PA_FP16) return false;
   if (block_size % kTile != 0) return false;

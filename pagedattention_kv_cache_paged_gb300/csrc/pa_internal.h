@@ -124,6 +124,11 @@ cudaError_t launch_lse_merge(const MergeArgs& a, pa_dtype dt, cudaStream_t s, in
 bool encode_pool_map(CUtensorMap* map, const void* pool, pa_dtype dt, int64_t num_blocks, int block_size,
                      int n_kv_heads, int head_dim, int64_t block_stride);
 
+// TMA view of the queries [total_q][n_q_heads][head_dim]: 3-D tensor (column, head, token), boxes of
+// 64 columns x heads_box heads x tokens_box tokens, 128-byte swizzle, rows past total_q read as zeros.
+bool encode_q_map(CUtensorMap* map, const void* q, pa_dtype dt, int64_t total_q, int n_q_heads, int head_dim,
+                  int heads_box, int tokens_box);
+
 // Tensor-core decode (TMA + mma.sync) for bf16/fp16 pools with block_size % 16 == 0.
 bool decode_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks);
 cudaError_t launch_decode_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);

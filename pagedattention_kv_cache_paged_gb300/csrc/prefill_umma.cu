@@ -7,20 +7,21 @@
 //
 // CTA = 256 (query token, head) rows of one KV head, split into two 128-row Q tiles that share
 // every K/V tile (kRows / G tokens x the G heads of the group: read-time GQA, nanoserve Day 19
-// "What I learned" 4).  10 warps:
+// "What I learned" 4).  11 warps:
 //   warps 0-3 / 4-7  softmax groups 0 / 1: thread t of group k owns row 128k + t (TMEM lane t of
-//              S_k and O_k); stages its Q row, turns each S_k tile into probabilities, rescales O_k
-//              in TMEM only when its stabilising maximum has to move up by more than 2^8, writes
-//              P_k (bf16/fp16) back into the TMEM columns of S_k, and normalises O_k at the end;
-//   warp 8     producer: lane 0 streams 128-key K tiles, lane 1 the matching V tiles (TMA boxes
-//              of 16 keys x 64 columns from the physical blocks the table names) into 2-stage
-//              rings;
-//   warp 9     MMA: allocates TMEM (S_0, S_1: 128 columns each; O_0, O_1: 128 columns each) and
+//              S_k and O_k); turns each S_k tile into probabilities, rescales O_k in TMEM only when
+//              its stabilising maximum has to move up by more than 2^8, writes P_k (bf16/fp16) back
+//              into the TMEM columns of S_k, and normalises O_k at the end;
+//   warp 8     K producer: loads both Q tiles (one TMA box per 64-column half), then streams 128-key
+//              K tiles (TMA boxes of 16 keys x 64 columns from the physical blocks the table names)
+//              into a 3-stage ring and publishes which sub-tiles hold data;
+//   warp 9     V producer: the matching V tiles into a 2-stage ring;
+//   warp 10    MMA: allocates TMEM (S_0, S_1: 128 columns each; O_0, O_1: 128 columns each) and
 //              issues S_k = Q_k K^T (M 128, N 128, both operands in shared memory) and
 //              O_k += P_k V (M 128, N head_dim, P read from TMEM, V an MN-major shared-memory
-//              operand) with tcgen05.mma as soon as each product's inputs are ready, so that the
-//              tensor core works on one group's products while the other group computes its
-//              softmax.  S_k of the next tile is issued only after O_k += P_k V of this one has
+//              operand) with tcgen05.mma in the order S_0(j), P_1(j-1) V, S_1(j), P_0(j) V, so
+//              that the tensor core works on one group's products while the other group computes
+//              its softmax.  S_k of the next tile is issued only after O_k += P_k V of this one has
 //              completed, because P_k lives in the columns the next S_k overwrites; that same
 //              ordering makes O_k stable whenever a group sees a new S_k, so rescaling needs no
 //              extra wait.
@@ -35,13 +36,13 @@
 
 namespace pa {
 
-constexpr int kUmThreads = 320;
+constexpr int kUmThreads = 352;            // 8 softmax warps, K producer, V producer, MMA
 constexpr int kUmTileRows = 128;            // rows per Q tile (MMA M)
 constexpr int kUmRows = 2 * kUmTileRows;    // rows per CTA
 constexpr int kUmKeys = 128;                // keys per K/V tile (N of S, K of PV)
 constexpr int kUmSub = kUmKeys / 16;
 constexpr int kUmTmemCols = 512;
-constexpr int kUmKStages = 2;               // K ring depth
+constexpr int kUmKStages = 3;               // K ring depth
 constexpr int kUmVStages = 2;               // V ring depth
 constexpr float kUmRescaleThreshold = 8.f;  // log2 units: O is rescaled when the max grows by > 2^8
 
@@ -65,65 +66,209 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c, int half_bytes) {
 // Keys whose bit is clear in mask[q] (chunk q = columns 32q .. 32q + 31) are outside the causal
 // bound or were not loaded; kMasked = false is the common case of a tile with every key valid.
 
-// Row maximum of the scaled scores.
-template <bool kMasked>
-__device__ __forceinline__ float s_row_max(uint32_t taddr, float sc, const uint32_t (&mask)[kUmKeys / 32]) {
+// Pairs out of every 8 whose exponentials run on the FMA pipe (exp2_fma) instead of the MUFU unit,
+// in unmasked tiles: at full tensor rate the MUFU alone would need as many cycles per tile as the
+// tensor core, so moving a share of the exponentials to the FMA pipe leaves it slack.
+#ifndef PA_UM_POLY_PAIRS
+#define PA_UM_POLY_PAIRS 0
+#endif
+constexpr int kUmPolyPairs = PA_UM_POLY_PAIRS;
+static_assert(kUmPolyPairs >= 0 && kUmPolyPairs <= 8, "pairs out of 8");
+
+// 2^x for a pair of arguments on the FMA pipe: Cody-Waite reduction x = n + f with n = round(x),
+// f in [-1/2, 1/2], then a degree-3 polynomial for 2^f (coefficients fitted to minimise the
+// relative error on [-1/2, 1/2]: at most 7.5e-5 in fp32, below half an ulp of bf16 and fp16) scaled
+// by 2^n built in the exponent field.  x is clamped below at -126 (2^-126 instead of a smaller
+// value: invisible next to a row sum of at least 1); a NaN argument gives NaN.
+__device__ __forceinline__ uint64_t exp2_fma2(float x0, float x1) {
+  constexpr float kRound = 12582912.f;  // 1.5 * 2^23: x + kRound holds round(x) in its low mantissa bits
+  constexpr float kC0 = 0.9999280571937561f, kC1 = 0.6932609677314758f, kC2 = 0.2426111251115799f,
+                  kC3 = 0.0551716648042202f;
+  float c0, c1;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(c0) : "f"(x0), "f"(-126.f));
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(c1) : "f"(x1), "f"(-126.f));
+  const uint64_t xc = f2_pack(c0, c1);
+  const uint64_t t = f2_add(xc, f2_pack(kRound, kRound));
+  const uint64_t f = f2_fma(f2_add(t, f2_pack(-kRound, -kRound)), f2_pack(-1.f, -1.f), xc);
+  uint64_t p = f2_fma(f2_pack(kC3, kC3), f, f2_pack(kC2, kC2));
+  p = f2_fma(p, f, f2_pack(kC1, kC1));
+  p = f2_fma(p, f, f2_pack(kC0, kC0));
+  float t0, t1;
+  f2_unpack(t, t0, t1);
+  // (bits of t) * 2^23 keeps n << 23 modulo 2^32; adding the bias gives the bits of 2^n
+  const uint32_t n0 = __float_as_uint(t0) * (1u << 23) + (127u << 23);
+  const uint32_t n1 = __float_as_uint(t1) * (1u << 23) + (127u << 23);
+  return f2_mul(p, f2_pack(__uint_as_float(n0), __uint_as_float(n1)));
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Columns [C0, C0 + N) of the row of S into registers: N / 32 loads in flight, one wait.
+template <int N, int C0>
+__device__ __forceinline__ void s_row_load(uint32_t taddr, uint32_t (&sv)[N]) {
+#pragma unroll
+  for (int q = 0; q < N / 32; ++q)
+    tmem_ld32(taddr + (uint32_t)(C0 + 32 * q), *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q]));
+  tmem_wait_ld();
+#pragma unroll
+  for (int q = 0; q < N / 32; ++q) tmem_pin32(*reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q]));
+}
+
+// Maximum of the scaled scores of keys [C0, C0 + N) (held in sv).  kMasked = false needs sc >= 0
+// (the maximum of the raw scores, scaled once).
+template <bool kMasked, int N, int C0>
+__device__ __forceinline__ float s_max(const uint32_t (&sv)[N], float sc, const uint32_t (&mask)[kUmKeys / 32]) {
   float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  if (!kMasked) {
 #pragma unroll
-  for (int q = 0; q < kUmKeys / 32; ++q) {
-    uint32_t v[32];
-    tmem_ld32(taddr + 32u * q, v);
-    tmem_wait_ld();
+    for (int j = 0; j < N; j += 8)
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      float x = __uint_as_float(v[j]) * sc;
-      if (kMasked) x = (mask[q] & (1u << j)) ? x : -INFINITY;
-      m[j & 3] = fmaxf(m[j & 3], x);
-    }
+      for (int u = 0; u < 4; ++u) m[u] = fmax3(m[u], __uint_as_float(sv[j + 2 * u]), __uint_as_float(sv[j + 2 * u + 1]));
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])) * sc;
+  }
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const int k = C0 + j;
+    const float x = ((mask[k >> 5] >> (k & 31)) & 1u) ? __uint_as_float(sv[j]) * sc : -INFINITY;
+    m[j & 3] = fmaxf(m[j & 3], x);
   }
   return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
-// Probabilities 2^(sc * s - m_sub) (0 for masked keys), written back as 16-bit pairs into the first
-// kUmKeys / 2 columns of the row (keys 2c and 2c + 1 in column c); returns their sum.  Columns
-// [32 h, 32 h + 32) of P hold keys [64 h, 64 h + 64), which are read before they are overwritten.
-template <bool kMasked, bool kBf16>
-__device__ __forceinline__ float p_row_store(uint32_t taddr, float sc, float m_sub,
-                                             const uint32_t (&mask)[kUmKeys / 32]) {
-  static_assert(kUmKeys == 128, "two halves of 64 keys");
+// Probabilities 2^(sc * s - m_sub) of keys [C0, C0 + N) (0 for masked keys), written back as 16-bit
+// pairs into columns [C0 / 2, (C0 + N) / 2) of the row (keys 2c and 2c + 1 in column c); returns
+// their sum.  Those columns were read into registers before, so the stores overwrite nothing still
+// needed.
+template <bool kMasked, bool kBf16, int N, int C0>
+__device__ __forceinline__ float p_store(uint32_t taddr, const uint32_t (&sv)[N], float sc, float m_sub,
+                                         const uint32_t (&mask)[kUmKeys / 32]) {
+  static_assert(N % 64 == 0 && C0 % 64 == 0, "whole 32-column stores");
+  if (!kMasked) {
+    // packed pairs: one f32x2 fma for the scaled, shifted arguments and one f32x2 add for the sum
+    const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(-m_sub, -m_sub);
+    uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+    for (int h = 0; h < N / 64; ++h) {
+      uint32_t w[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int j = 64 * h + 2 * c;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])), sc2, nm2), x0, x1);
+        uint64_t e2;
+        if ((c & 7) < kUmPolyPairs)
+          e2 = exp2_fma2(x0, x1);
+        else
+          e2 = f2_pack(fast_exp2(x0), fast_exp2(x1));
+        acc2[c & 1] = f2_add(acc2[c & 1], e2);
+        float e0, e1;
+        f2_unpack(e2, e0, e1);
+        w[c] = pack2<kBf16>(e0, e1);
+      }
+      tmem_st32(taddr + (uint32_t)(C0 / 2 + 32 * h), w);
+    }
+    float a0, a1, b0, b1;
+    f2_unpack(acc2[0], a0, a1);
+    f2_unpack(acc2[1], b0, b1);
+    return (a0 + b0) + (a1 + b1);
+  }
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1  // one half at a time keeps the register footprint at one chunk in, one chunk out
-  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+  for (int h = 0; h < N / 64; ++h) {
     uint32_t w[32];
 #pragma unroll
-    for (int q2 = 0; q2 < 2; ++q2) {
-      const int q = 2 * h + q2;
-      const uint32_t mq = h == 0 ? mask[q2] : mask[2 + q2];
-      uint32_t v[32];
-      tmem_ld32(taddr + 32u * q, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        float e0 = fast_exp2(fmaf(__uint_as_float(v[j]), sc, -m_sub));
-        float e1 = fast_exp2(fmaf(__uint_as_float(v[j + 1]), sc, -m_sub));
-        if (kMasked) {
-          e0 = (mq & (1u << j)) ? e0 : 0.f;
-          e1 = (mq & (2u << j)) ? e1 : 0.f;
-        }
-        acc[j & 3] += e0;
-        acc[(j + 1) & 3] += e1;
-        w[16 * q2 + j / 2] = pack2<kBf16>(e0, e1);
-      }
+    for (int c = 0; c < 32; ++c) {
+      const int j = 64 * h + 2 * c;
+      const int k = C0 + j;
+      const uint32_t mq = mask[k >> 5];
+      float e0 = fast_exp2(fmaf(__uint_as_float(sv[j]), sc, -m_sub));
+      float e1 = fast_exp2(fmaf(__uint_as_float(sv[j + 1]), sc, -m_sub));
+      e0 = ((mq >> (k & 31)) & 1u) ? e0 : 0.f;
+      e1 = ((mq >> ((k + 1) & 31)) & 1u) ? e1 : 0.f;
+      acc[c & 3] += e0 + e1;
+      w[c] = pack2<kBf16>(e0, e1);
     }
-    tmem_st32(taddr + 32u * h, w);
+    tmem_st32(taddr + (uint32_t)(C0 / 2 + 32 * h), w);
   }
   return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
+// How the softmax reads a row of S: 1 = all kUmKeys columns with one wait (then the row stays in
+// registers for the exponentials), 2 = two halves for the maximum and the same two halves again
+// for the exponentials (half the registers, four waits).
+#ifndef PA_UM_ROW_SPLIT
+#define PA_UM_ROW_SPLIT 2
+#endif
+static_assert(PA_UM_ROW_SPLIT == 1 || PA_UM_ROW_SPLIT == 2, "row split");
+
+// Row maximum and probabilities of one S tile (see s_max / p_store); moves the stabilising maximum
+// m_use when it has to and returns the factor the earlier sum and O must be scaled by.
+template <bool kMasked, bool kBf16>
+__device__ __forceinline__ float row_softmax(uint32_t srow, float sc, const uint32_t (&mask)[kUmKeys / 32],
+                                             float& m_use, float& l_run) {
+  static_assert(kUmKeys == 128, "two halves of 64 keys");
+  float mx;
+#if PA_UM_ROW_SPLIT == 1
+  uint32_t sv[kUmKeys];
+  s_row_load<kUmKeys, 0>(srow, sv);
+  mx = s_max<kMasked, kUmKeys, 0>(sv, sc, mask);
+#else
+  {
+    uint32_t sv[64];
+    s_row_load<64, 0>(srow, sv);
+    mx = s_max<kMasked, 64, 0>(sv, sc, mask);
+    s_row_load<64, 64>(srow, sv);
+    mx = fmaxf(mx, s_max<kMasked, 64, 64>(sv, sc, mask));
+  }
+#endif
+  // move the stabiliser only when it must: first finite maximum, or growth beyond 2^8
+  float corr = 1.f;
+  if (mx > m_use + kUmRescaleThreshold || (m_use == -INFINITY && mx != -INFINITY)) {
+    corr = fast_exp2(m_use - mx);  // m_use = -inf -> 0
+    m_use = mx;
+  }
+  const float m_sub = m_use == -INFINITY ? 0.f : m_use;
+#if PA_UM_ROW_SPLIT == 1
+  const float rs = p_store<kMasked, kBf16, kUmKeys, 0>(srow, sv, sc, m_sub, mask);
+#else
+  float rs;
+  {
+    uint32_t sv[64];
+    s_row_load<64, 0>(srow, sv);
+    rs = p_store<kMasked, kBf16, 64, 0>(srow, sv, sc, m_sub, mask);
+    s_row_load<64, 64>(srow, sv);
+    rs += p_store<kMasked, kBf16, 64, 64>(srow, sv, sc, m_sub, mask);
+  }
+#endif
+  l_run = l_run * corr + rs;
+  return corr;
+}
+
+// Sequence of query row t: the largest b < batch with qsl[b] <= t, searched by the whole warp with
+// 32 candidates per round (two rounds of loads for batch <= 1024).  Every lane gets the answer.
+__device__ __forceinline__ int find_sequence_warp(const int32_t* qsl, int batch, int t) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, n = batch;
+  while (n > 1) {
+    const int step = (n + 31) >> 5;
+    const bool le = lane * step < n && __ldg(qsl + lo + lane * step) <= t;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    const int top = m ? 31 - __clz((int)m) : 0;
+    const int nlo = lo + top * step;
+    n = min(step, lo + n - nlo);
+    lo = nlo;
+  }
+  return lo;
+}
+
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kUmThreads, 1)
+__global__ void __launch_bounds__(kUmThreads)
     prefill_umma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap) {
+                        const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap) {
   using Cfg = UmCfg<D>;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr int kHalves = Cfg::kHalves;
@@ -136,7 +281,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   uint64_t* kempty = bars + 4;    // [kUmKStages] completes when both groups' S products have read the tile
   uint64_t* vfull = bars + 8;     // [kUmVStages]
   uint64_t* vempty = bars + 12;   // [kUmVStages] completes when both groups' P V products have read the tile
-  uint64_t* q_ready = bars + 16;
+  uint64_t* q_ready = bars + 16;  // both Q tiles landed
   // per group k, one phase per tile
   uint64_t* s_full = bars + 17;   // [2] S_k computed (and, with it, every earlier product of the CTA)
   uint64_t* p_full = bars + 19;   // [2] P_k written to TMEM (and O_k rescaled)
@@ -146,40 +291,43 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 512);
   uint32_t* kmask = reinterpret_cast<uint32_t*>(base + 768);  // [8] sub-tiles holding data, per tile slot
   uint8_t* qs = base + 1024;                       // [2][Q tile]
-  uint8_t* ks = qs + 2 * Cfg::kQBytes;             // [3 stages][K tile]
-  uint8_t* vs = ks + kUmKStages * Cfg::kKvBytes;   // [2 stages][V tile]
+  uint8_t* ks = qs + 2 * Cfg::kQBytes;             // [kUmKStages][K tile]
+  uint8_t* vs = ks + kUmKStages * Cfg::kKvBytes;   // [kUmVStages][V tile]
+  static_assert(kUmKStages <= 4 && kUmVStages <= 4, "barrier slots");
 
   const int kvh = blockIdx.x % a.n_kv_heads;
-  const int64_t T0 = (int64_t)(blockIdx.x / a.n_kv_heads) * kQB;
-  const int64_t T1 = min(T0 + kQB, a.rows);
+  // query rows, positions and lengths all fit in int32 (query_start_loc and context_lens are int32)
+  const int T0 = (int)(blockIdx.x / a.n_kv_heads) * kQB;
+  const int T1 = (int)min((int64_t)T0 + kQB, a.rows);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t max_len = a.bt_stride << a.block_shift;
+  const int max_len = (int)min(a.bt_stride << a.block_shift, (int64_t)INT32_MAX);
   const int bmask = a.block_size - 1;
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
+    prefetch_tensormap(&qmap);
+    // one commit per tile closes a K (V) stage: it follows both groups' S (P V) products of the tile
     for (int s = 0; s < kUmKStages; ++s) {
       mbar_init(&kfull[s], 1);
-      mbar_init(&kempty[s], 2);
+      mbar_init(&kempty[s], 1);
     }
     for (int s = 0; s < kUmVStages; ++s) {
       mbar_init(&vfull[s], 1);
-      mbar_init(&vempty[s], 2);
+      mbar_init(&vempty[s], 1);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(&s_full[k], 1);
       mbar_init(&p_full[k], 128);
       mbar_init(&pv_done[k], 1);
     }
-    mbar_init(q_ready, 256);
+    mbar_init(q_ready, 1);
     mbar_init(fin, 1);
     for (int s = 0; s < 8; ++s) mbar_init(&mready[s], 1);
     fence_barrier_init();
-    fence_proxy_async_smem();
   }
-  if (warp == 9) tmem_alloc(tmem_slot, kUmTmemCols);
+  if (warp == 10) tmem_alloc(tmem_slot, kUmTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -191,19 +339,20 @@ __global__ void __launch_bounds__(kUmThreads, 1)
 
   struct Seg {
     int b;
-    int64_t seg1, n, pos0, q0, kv_end;
+    int seg1, n, pos0, q0, kv_end;
     bool ok;
   };
-  auto segment_at = [&](int64_t t) -> Seg {
+  // the rows [t, seg1) of this CTA that belong to the sequence holding row t (warp-collective)
+  auto segment_at = [&](int t) -> Seg {
     Seg sg;
-    const int b = find_sequence(a.query_start_loc, a.batch, t);
-    const int64_t q0 = __ldg(a.query_start_loc + b);
-    const int64_t q1 = __ldg(a.query_start_loc + b + 1);
-    int64_t n = __ldg(a.context_lens + b);
+    const int b = find_sequence_warp(a.query_start_loc, a.batch, t);
+    const int q0 = __ldg(a.query_start_loc + b);
+    const int q1 = __ldg(a.query_start_loc + b + 1);
+    int n = __ldg(a.context_lens + b);
     sg.b = b;
     sg.seg1 = min(q1, T1);
     if (sg.seg1 <= t) sg.seg1 = t + 1;
-    sg.ok = q0 <= t && t < q1 && n >= q1 - q0 && n <= max_len;
+    sg.ok = q0 <= t && t < q1 && (int64_t)n >= (int64_t)q1 - q0 && n <= max_len;
     if (!sg.ok) n = 0;
     sg.n = n;
     sg.q0 = q0;
@@ -211,85 +360,105 @@ __global__ void __launch_bounds__(kUmThreads, 1)
     sg.kv_end = sg.ok ? sg.pos0 + (sg.seg1 - 1 - q0) + 1 : 0;
     return sg;
   };
-  auto tiles_of = [](const Seg& sg) -> int { return (int)((sg.kv_end + kUmKeys - 1) / kUmKeys); };
+  auto tiles_of = [](const Seg& sg) -> int { return (sg.kv_end + kUmKeys - 1) / kUmKeys; };
 
-  if (warp == 8) {
-    // --------------------------- producer: lane 0 -> K tiles, lane 1 -> V tiles --------------------
-    if (lane < 2) {
-      const bool is_v = lane == 1;
-      uint64_t* full = is_v ? vfull : kfull;
-      uint64_t* empty = is_v ? vempty : kempty;
-      uint8_t* ring = is_v ? vs : ks;
-      const CUtensorMap* map = is_v ? &vmap : &kmap;
-      const int depth = is_v ? kUmVStages : kUmKStages;
-      int i = 0;
-      bool alive = true;
-      for (int64_t t = T0; t < T1 && alive;) {
-        const Seg sg = segment_at(t);
-        const int32_t* table = a.block_table + (int64_t)sg.b * a.bt_stride;
-        const int nt = tiles_of(sg);
-        for (int tile = 0; tile < nt; ++tile, ++i) {
+  if (warp == 8 || warp == 9) {
+    // ---------------- producers: warp 8 streams K tiles (and the Q tiles), warp 9 V tiles ----------------
+    const bool is_v = warp == 9;
+    uint64_t* full = is_v ? vfull : kfull;
+    uint64_t* empty = is_v ? vempty : kempty;
+    uint8_t* ring = is_v ? vs : ks;
+    const CUtensorMap* map = is_v ? &vmap : &kmap;
+    const int depth = is_v ? kUmVStages : kUmKStages;
+    if (!is_v && lane == 0) {
+      // both Q tiles: rows (token, head) of the G heads of this KV head, one box per 64-column half
+      mbar_arrive_expect_tx(q_ready, 2 * Cfg::kQBytes);
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h)
+          tma_load_3d(qs + k * Cfg::kQBytes + h * Cfg::kQHalf, &qmap, h * 64, kvh * G, T0 + k * (kUmTileRows / G),
+                      q_ready);
+    }
+    int i = 0;
+    bool alive = true;
+    for (int t = T0; t < T1 && alive;) {
+      const Seg sg = segment_at(t);
+      const int32_t* table = a.block_table + (int64_t)sg.b * a.bt_stride;
+      const int nt = tiles_of(sg);
+      for (int tile = 0; tile < nt; ++tile, ++i) {
+        bool ok = true;
+        if (lane == 0) {
           const int s = i % depth;
           const int round = i / depth;
-          if (round > 0 && !mbar_wait(&empty[s], (unsigned)((round - 1) & 1), a.err)) {
-            raise_error(a.err, PA_DEVERR_TIMEOUT);
-            alive = false;
-            break;
-          }
-          int ys[kUmSub], yo[kUmSub];
-          uint32_t bytes = 0;
+          ok = round == 0 || mbar_wait(&empty[s], (unsigned)((round - 1) & 1), a.err);
+          if (ok) {
+            int ys[kUmSub], yo[kUmSub];
+            unsigned m = 0;
 #pragma unroll
-          for (int sub = 0; sub < kUmSub; ++sub) {
-            const int64_t k0 = (int64_t)tile * kUmKeys + sub * 16;
-            ys[sub] = -1;
-            if (k0 < sg.kv_end) {
-              const int blk = __ldg(table + (k0 >> a.block_shift));
-              if (blk < 0 || blk >= a.num_blocks) {
-                if (!is_v) raise_error(a.err, PA_DEVERR_BLOCK_ID);
-              } else {
-                ys[sub] = blk;
-                yo[sub] = (int)(k0 & bmask);
-                bytes += kHalves * 2048;
+            for (int sub = 0; sub < kUmSub; ++sub) {
+              const int k0 = tile * kUmKeys + sub * 16;
+              ys[sub] = -1;
+              yo[sub] = 0;
+              if (k0 < sg.kv_end) {
+                const int blk = __ldg(table + (k0 >> a.block_shift));
+                if (blk < 0 || blk >= a.num_blocks) {
+                  if (!is_v) raise_error(a.err, PA_DEVERR_BLOCK_ID);
+                } else {
+                  ys[sub] = blk;
+                  yo[sub] = k0 & bmask;
+                  m |= 1u << sub;
+                }
+              }
+            }
+            if (!is_v) {
+              // publish which sub-tiles hold data; the softmax groups read it instead of the table.
+              // Slot i % 8 was last read for tile i - 8, which both groups finished long ago: K tile
+              // i is loaded only after both S products of tile i - kUmKStages completed, which
+              // needed each group's P of tile i - kUmKStages - 1.
+              kmask[i & 7] = m;
+              mbar_arrive(&mready[i & 7]);
+            }
+            uint8_t* st = ring + s * Cfg::kKvBytes;
+            if (m == 0) {
+              mbar_arrive(&full[s]);
+            } else {
+              mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(m) * kHalves * 2048u);
+#pragma unroll
+              for (int sub = 0; sub < kUmSub; ++sub) {
+                if (ys[sub] < 0) continue;
+#pragma unroll
+                for (int h = 0; h < kHalves; ++h)
+                  tma_load_3d(st + h * Cfg::kKvHalf + sub * 2048, map, kvh * D + h * 64, yo[sub], ys[sub], &full[s]);
               }
             }
           }
-          if (!is_v) {
-            // publish which sub-tiles hold data; the softmax groups read it instead of the table.
-            // Slot i % 8 was last read for tile i - 8, which both groups finished long ago: K tile
-            // i is loaded only after both S products of tile i - 2 completed, which needed each
-            // group's P of tile i - 3.
-            unsigned m = 0;
-#pragma unroll
-            for (int sub = 0; sub < kUmSub; ++sub) m |= (ys[sub] >= 0 ? 1u : 0u) << sub;
-            kmask[i & 7] = m;
-            mbar_arrive(&mready[i & 7]);
-          }
-          uint8_t* st = ring + s * Cfg::kKvBytes;
-          if (bytes == 0) {
-            mbar_arrive(&full[s]);
-          } else {
-            mbar_arrive_expect_tx(&full[s], bytes);
-#pragma unroll
-            for (int sub = 0; sub < kUmSub; ++sub) {
-              if (ys[sub] < 0) continue;
-#pragma unroll
-              for (int h = 0; h < kHalves; ++h)
-                tma_load_3d(st + h * Cfg::kKvHalf + sub * 2048, map, kvh * D + h * 64, yo[sub], ys[sub], &full[s]);
-            }
-          }
         }
-        t = sg.seg1;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+          alive = false;
+          break;
+        }
       }
+      t = sg.seg1;
     }
-  } else if (warp == 9) {
-    // ------------------------------------------ MMA ---------------------------------------------
+    // Leave no copy in flight: after a normal run every issued tile was consumed and these waits
+    // return at once; after a timeout elsewhere they wait (bounded) for this ring's last tiles.
     if (lane == 0) {
-      int n_all = 0;
-      for (int64_t t = T0; t < T1;) {
-        const Seg sg = segment_at(t);
-        n_all += tiles_of(sg);
-        t = sg.seg1;
-      }
+      const int issued = i;  // a tile whose wait failed was not issued and not counted
+      for (int k = issued > depth ? issued - depth : 0; k < issued; ++k)
+        mbar_wait(&full[k % depth], (unsigned)((k / depth) & 1));
+      if (!is_v) mbar_wait(q_ready, 0);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------ MMA ---------------------------------------------
+    int n_all = 0;
+    for (int t = T0; t < T1;) {
+      const Seg sg = segment_at(t);
+      n_all += tiles_of(sg);
+      t = sg.seg1;
+    }
+    if (lane == 0) {
       const uint32_t id_s = umma_idesc_f16(kBf16, 128, kUmKeys, false, false);
       const uint32_t id_pv = umma_idesc_f16(kBf16, 128, D, false, true);
       auto issue_s = [&](int k, int i) {
@@ -313,45 +482,36 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                   (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&pv_done[k]);
       };
-      // Event-driven issue: each group's next S (needs the K tile and its previous P V finished) and
-      // next P V (needs its P and the V tile) are issued as soon as they are ready, so a slow group
-      // never holds back the other group's products.
+      // Fixed issue order per tile j: S_0(j), P_1(j-1) V, S_1(j), P_0(j) V.  While group 0 turns
+      // S_0(j) into P_0(j) the tensor core runs group 1's P V and next S, and the other way round.
+      // S_k(j) overwrites P_k(j-1), so it waits for O_k += P_k(j-1) V to complete.  The waits
+      // suspend the thread instead of polling, leaving issue slots to the softmax warps.
       bool alive = mbar_wait(q_ready, 0, a.err);
-      int next_s[2] = {0, 0}, next_pv[2] = {0, 0};
-      int idle = 0;
-      while (alive && (next_pv[0] < n_all || next_pv[1] < n_all)) {
-        bool progress = false;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          // S_k(j) overwrites P_k(j - 1): O_k += P_k(j - 1) V must have completed
-          const int j = next_s[k];
-          if (j < n_all && j == next_pv[k] && (j == 0 || mbar_test(&pv_done[k], (unsigned)((j - 1) & 1))) &&
-              mbar_test(&kfull[j % kUmKStages], (unsigned)((j / kUmKStages) & 1))) {
-            tc_fence_after();
-            issue_s(k, j);
-            umma_commit(&kempty[j % kUmKStages]);
-            next_s[k] = j + 1;
-            progress = true;
-          }
-          const int jp = next_pv[k];
-          // group 1's P V follows group 0's for the same tile: group 0 zeroes the tile's stale V
-          // rows before it signals p_full, and group 1 must not read them earlier
-          if (jp < next_s[k] && (k == 0 || next_pv[0] > jp) && mbar_test(&p_full[k], (unsigned)(jp & 1)) &&
-              mbar_test(&vfull[jp % kUmVStages], (unsigned)((jp / kUmVStages) & 1))) {
-            tc_fence_after();
-            issue_pv(k, jp);
-            umma_commit(&vempty[jp % kUmVStages]);
-            next_pv[k] = jp + 1;
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle = 0;
-        } else if (++idle > kWaitSpins ||
-                   (idle > 4096 && (*reinterpret_cast<const volatile unsigned*>(a.err) & PA_DEVERR_TIMEOUT))) {
-          alive = false;
-        }
+      auto wait = [&](uint64_t* bar, unsigned parity) {
+        alive = alive && mbar_wait(bar, parity, a.err);
+        return alive;
+      };
+      auto pv_of = [&](int k, int j) {  // O_k += P_k(j) V(j); group 1's closes V tile j
+        if (!wait(&p_full[k], (unsigned)(j & 1)) || !wait(&vfull[j % kUmVStages], (unsigned)((j / kUmVStages) & 1)))
+          return false;
+        tc_fence_after();
+        issue_pv(k, j);
+        if (k == 1) umma_commit(&vempty[j % kUmVStages]);
+        return true;
+      };
+      for (int j = 0; j < n_all && alive; ++j) {
+        if (!wait(&kfull[j % kUmKStages], (unsigned)((j / kUmKStages) & 1))) break;
+        if (j > 0 && !wait(&pv_done[0], (unsigned)((j - 1) & 1))) break;
+        tc_fence_after();
+        issue_s(0, j);
+        if (j > 0 && !pv_of(1, j - 1)) break;
+        if (j > 0 && !wait(&pv_done[1], (unsigned)((j - 1) & 1))) break;
+        tc_fence_after();
+        issue_s(1, j);
+        umma_commit(&kempty[j % kUmKStages]);
+        if (!pv_of(0, j)) break;
       }
+      if (alive && n_all > 0) pv_of(1, n_all - 1);
       if (!alive) raise_error(a.err, PA_DEVERR_TIMEOUT);
       if (n_all > 0) {
         umma_commit(fin);
@@ -363,31 +523,20 @@ __global__ void __launch_bounds__(kUmThreads, 1)
     const int grp = warp >> 2;           // 0 or 1
     const int r = threadIdx.x & 127;     // row inside the Q tile = TMEM lane
     const int row = grp * kUmTileRows + r;
-    const int64_t tok = T0 + row / G;
+    const int tok = T0 + row / G;
     const int head = kvh * G + row % G;
-    uint8_t* q_tile = qs + grp * Cfg::kQBytes;
-    {
-      const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + (tok * a.n_q_heads + head) * D);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = tok < T1 ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(q_tile + sw_off(r, c, Cfg::kQHalf)) = v;
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(q_ready);
-    }
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     float m_use = -INFINITY;  // stabilising maximum (log2 domain) the exponentials are taken against
     float l_run = 0.f;
     int i = 0;
     bool alive = true;
-    for (int64_t t = T0; t < T1 && alive;) {
+    for (int t = T0; t < T1 && alive;) {
       const Seg sg = segment_at(t);
       if (!sg.ok && threadIdx.x == 0) raise_error(a.err, PA_DEVERR_QUERY_LOC);
-      const int64_t bound = (sg.ok && tok >= t && tok < sg.seg1) ? sg.pos0 + (tok - sg.q0) : -1;
+      const int bound = (sg.ok && tok >= t && tok < sg.seg1) ? sg.pos0 + (tok - sg.q0) : -1;
       const int nt = tiles_of(sg);
       for (int tile = 0; tile < nt; ++tile, ++i) {
-        const int64_t kb = (int64_t)tile * kUmKeys;
+        const int kb = tile * kUmKeys;
         if (!__all_sync(0xffffffffu, mbar_wait(&mready[i & 7], (unsigned)((i >> 3) & 1), a.err))) {
           alive = false;
           break;
@@ -406,7 +555,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         const bool unmasked = __all_sync(0xffffffffu, loaded == all_sub && kb + kUmKeys - 1 <= bound);
         uint32_t mask[kUmKeys / 32];
         {
-          const int64_t lim = bound - kb;  // keys c <= lim are causal
+          const int lim = bound - kb;  // keys c <= lim are causal
           const int nv = lim < 0 ? 0 : (lim >= kUmKeys ? kUmKeys : (int)lim + 1);
 #pragma unroll
           for (int q = 0; q < kUmKeys / 32; ++q) {
@@ -418,24 +567,14 @@ __global__ void __launch_bounds__(kUmThreads, 1)
           }
         }
         const uint32_t srow = tS(grp) + lane_base;
-        const float mx = unmasked ? s_row_max<false>(srow, sc, mask) : s_row_max<true>(srow, sc, mask);
-        // move the stabiliser only when it must: first finite maximum, or growth beyond 2^8
-        float corr = 1.f;
-        if (mx > m_use + kUmRescaleThreshold || (m_use == -INFINITY && mx != -INFINITY)) {
-          corr = fast_exp2(m_use - mx);  // m_use = -inf -> 0
-          m_use = mx;
-        }
-        const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-        const float rs = unmasked ? p_row_store<false, kBf16>(srow, sc, m_sub, mask)
-                                  : p_row_store<true, kBf16>(srow, sc, m_sub, mask);
-        l_run = l_run * corr + rs;
+        const float corr = (unmasked && sc >= 0.f) ? row_softmax<false, kBf16>(srow, sc, mask, m_use, l_run)
+                                                   : row_softmax<true, kBf16>(srow, sc, mask, m_use, l_run);
         // O_k is stable here (its last product completed before this S_k was issued)
         if (i > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32(tO(grp) + lane_base + c0, v);
-            tmem_wait_ld();
+            tmem_ld32_sync(tO(grp) + lane_base + c0, v);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * corr);
             tmem_st32(tO(grp) + lane_base + c0, v);
@@ -470,12 +609,11 @@ __global__ void __launch_bounds__(kUmThreads, 1)
     }
     const bool have = alive && i > 0 && l_run != 0.f;
     const float inv = have ? 1.f / l_run : 0.f;
-    T* orow = static_cast<T*>(a.out) + (tok * a.n_q_heads + head) * D;
+    T* orow = static_cast<T*>(a.out) + ((int64_t)tok * a.n_q_heads + head) * D;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t v[32];
-      tmem_ld32(tO(grp) + lane_base + c0, v);
-      tmem_wait_ld();
+      tmem_ld32_sync(tO(grp) + lane_base + c0, v);
       if (tok < T1) {
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
@@ -494,7 +632,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 10) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kUmTmemCols);
@@ -505,6 +643,10 @@ __global__ void __launch_bounds__(kUmThreads, 1)
 
 template <typename T, int D, int G>
 static cudaError_t launch_um_g(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
+  CUtensorMap qm;
+  if (!encode_q_map(&qm, a.q, std::is_same<T, __nv_bfloat16>::value ? PA_BF16 : PA_FP16, a.rows, a.n_q_heads, D, G,
+                    kUmTileRows / G))
+    return cudaErrorInvalidValue;
   constexpr int smem = UmCfg<D>::kSmemBytes;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -519,7 +661,7 @@ static cudaError_t launch_um_g(const AttnArgs& a, const CUtensorMap& km, const C
   const int64_t grid = ((a.rows + qb - 1) / qb) * a.n_kv_heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  prefill_umma_kernel<T, D, G><<<(unsigned)grid, kUmThreads, smem, s>>>(a, km, vm);
+  prefill_umma_kernel<T, D, G><<<(unsigned)grid, kUmThreads, smem, s>>>(a, km, vm, qm);
   return cudaGetLastError();
 }
 
