@@ -1,6 +1,7 @@
 // Inline-PTX wrappers for the pipelined kernels: mbarrier, TMA (cp.async.bulk.tensor), ldmatrix
-// and mma.sync.  Every wait on an mbarrier is bounded: callers get `false` back after
-// kWaitSpins unsuccessful polls and must record PA_DEVERR_TIMEOUT and leave.
+// and mma.sync.  Every wait on an mbarrier is bounded: callers get `false` back after about
+// kWaitLimitNs without the phase completing (or once another CTA has given up) and must record
+// PA_DEVERR_TIMEOUT and leave.
 #pragma once
 
 #include <cuda.h>
@@ -8,7 +9,14 @@
 
 namespace pa {
 
-constexpr int kWaitSpins = 1 << 22;
+// Between unsuccessful tries a waiting thread sleeps about kWaitSleepNs (nanosleep), so waiting
+// warps take few issue slots from the working warps of their SM sub-partition; a wait gives up
+// after kWaitLimitNs of global time.
+#ifndef PA_WAIT_SLEEP_NS
+#define PA_WAIT_SLEEP_NS 32
+#endif
+constexpr unsigned kWaitSleepNs = PA_WAIT_SLEEP_NS;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -62,17 +70,28 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, unsigned parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.  After a short spin the wait also
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase with the given parity to complete.  Between tries the wait also
 // watches `abort_word` (the device error word): once any CTA has recorded a timeout, the others stop
 // waiting too, so a broken launch ends after about one timeout period instead of one per CTA.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, const unsigned* abort_word = nullptr) {
-  for (int i = 0; i < kWaitSpins; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (unsigned n = 1;; ++n) {
+    if (kWaitSleepNs) __nanosleep(kWaitSleepNs);
     if (mbar_try_wait(bar, parity)) return true;
-    if (abort_word != nullptr && i >= 4096 && (i & 1023) == 0 &&
-        (*reinterpret_cast<const volatile unsigned*>(abort_word) & 32u /* PA_DEVERR_TIMEOUT */))
-      return false;
+    if ((n & 15u) == 0) {
+      if (abort_word != nullptr &&
+          (*reinterpret_cast<const volatile unsigned*>(abort_word) & 32u /* PA_DEVERR_TIMEOUT */))
+        return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
   }
-  return false;
 }
 
 // 2-D tiled TMA load global -> shared, completing `bytes` on `bar`.  x is the inner coordinate.
