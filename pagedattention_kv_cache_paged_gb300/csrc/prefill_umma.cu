@@ -30,6 +30,8 @@
 // same one, so the result equals the running-max form of "Online Softmax" in real arithmetic.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
@@ -45,6 +47,11 @@ constexpr int kUmTmemCols = 512;
 constexpr int kUmKStages = 3;               // K ring depth
 constexpr int kUmVStages = 2;               // V ring depth
 constexpr float kUmRescaleThreshold = 8.f;  // log2 units: O is rescaled when the max grows by > 2^8
+// 1: one CTA per SM walking the work items; 0: one CTA per work item
+#ifndef PA_UM_PERSISTENT
+#define PA_UM_PERSISTENT 1
+#endif
+constexpr bool kUmPersistent = PA_UM_PERSISTENT != 0;
 
 template <int D>
 struct UmCfg {
@@ -281,13 +288,15 @@ __global__ void __launch_bounds__(kUmThreads)
   uint64_t* kempty = bars + 4;    // [kUmKStages] completes when both groups' S products have read the tile
   uint64_t* vfull = bars + 8;     // [kUmVStages]
   uint64_t* vempty = bars + 12;   // [kUmVStages] completes when both groups' P V products have read the tile
-  uint64_t* q_ready = bars + 16;  // both Q tiles landed
+  uint64_t* q_ready = bars + 16;  // one phase per work item: both Q tiles landed
   // per group k, one phase per tile
   uint64_t* s_full = bars + 17;   // [2] S_k computed (and, with it, every earlier product of the CTA)
   uint64_t* p_full = bars + 19;   // [2] P_k written to TMEM (and O_k rescaled)
   uint64_t* pv_done = bars + 21;  // [2] O_k += P_k V finished
   uint64_t* fin = bars + 23;
   uint64_t* mready = bars + 24;   // [8] per tile slot: the sub-tile mask below is written
+  uint64_t* q_empty = bars + 32;  // one phase per work item: its S products completed, Q may be reloaded
+  uint64_t* o_free = bars + 33;   // [2] one phase per work item: group k has read O_k
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 512);
   uint32_t* kmask = reinterpret_cast<uint32_t*>(base + 768);  // [8] sub-tiles holding data, per tile slot
   uint8_t* qs = base + 1024;                       // [2][Q tile]
@@ -295,10 +304,11 @@ __global__ void __launch_bounds__(kUmThreads)
   uint8_t* vs = ks + kUmKStages * Cfg::kKvBytes;   // [kUmVStages][V tile]
   static_assert(kUmKStages <= 4 && kUmVStages <= 4, "barrier slots");
 
-  const int kvh = blockIdx.x % a.n_kv_heads;
-  // query rows, positions and lengths all fit in int32 (query_start_loc and context_lens are int32)
-  const int T0 = (int)(blockIdx.x / a.n_kv_heads) * kQB;
-  const int T1 = (int)min((int64_t)T0 + kQB, a.rows);
+  // Work items are (block of kQB query tokens, KV head) pairs; this CTA takes items blockIdx.x,
+  // blockIdx.x + gridDim.x, ...  Query rows, positions and lengths all fit in int32
+  // (query_start_loc and context_lens are int32).
+  const int rows = (int)a.rows;
+  const int n_items = (rows + kQB - 1) / kQB * a.n_kv_heads;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int max_len = (int)min(a.bt_stride << a.block_shift, (int64_t)INT32_MAX);
@@ -321,8 +331,10 @@ __global__ void __launch_bounds__(kUmThreads)
       mbar_init(&s_full[k], 1);
       mbar_init(&p_full[k], 128);
       mbar_init(&pv_done[k], 1);
+      mbar_init(&o_free[k], 128);
     }
     mbar_init(q_ready, 1);
+    mbar_init(q_empty, 1);
     mbar_init(fin, 1);
     for (int s = 0; s < 8; ++s) mbar_init(&mready[s], 1);
     fence_barrier_init();
@@ -342,8 +354,8 @@ __global__ void __launch_bounds__(kUmThreads)
     int seg1, n, pos0, q0, kv_end;
     bool ok;
   };
-  // the rows [t, seg1) of this CTA that belong to the sequence holding row t (warp-collective)
-  auto segment_at = [&](int t) -> Seg {
+  // the rows [t, seg1) of rows [t, T1) that belong to the sequence holding row t (warp-collective)
+  auto segment_at = [&](int t, int T1) -> Seg {
     Seg sg;
     const int b = find_sequence_warp(a.query_start_loc, a.batch, t);
     const int q0 = __ldg(a.query_start_loc + b);
@@ -363,75 +375,33 @@ __global__ void __launch_bounds__(kUmThreads)
   auto tiles_of = [](const Seg& sg) -> int { return (sg.kv_end + kUmKeys - 1) / kUmKeys; };
 
   if (warp == 8 || warp == 9) {
-    // ---------------- producers: warp 8 streams K tiles (and the Q tiles), warp 9 V tiles ----------------
+    // ------- producers: warp 8 streams K tiles; warp 9 each item's Q tiles, then its V tiles -------
     const bool is_v = warp == 9;
     uint64_t* full = is_v ? vfull : kfull;
     uint64_t* empty = is_v ? vempty : kempty;
     uint8_t* ring = is_v ? vs : ks;
     const CUtensorMap* map = is_v ? &vmap : &kmap;
     const int depth = is_v ? kUmVStages : kUmKStages;
-    if (!is_v && lane == 0) {
-      // both Q tiles: rows (token, head) of the G heads of this KV head, one box per 64-column half
-      mbar_arrive_expect_tx(q_ready, 2 * Cfg::kQBytes);
-#pragma unroll
-      for (int k = 0; k < 2; ++k)
-#pragma unroll
-        for (int h = 0; h < kHalves; ++h)
-          tma_load_3d(qs + k * Cfg::kQBytes + h * Cfg::kQHalf, &qmap, h * 64, kvh * G, T0 + k * (kUmTileRows / G),
-                      q_ready);
-    }
-    int i = 0;
+    int i = 0;      // tiles issued, counted over all items of the CTA
+    int nq = 0;     // Q loads issued
     bool alive = true;
-    for (int t = T0; t < T1 && alive;) {
-      const Seg sg = segment_at(t);
-      const int32_t* table = a.block_table + (int64_t)sg.b * a.bt_stride;
-      const int nt = tiles_of(sg);
-      for (int tile = 0; tile < nt; ++tile, ++i) {
+    for (int w = blockIdx.x; w < n_items && alive; w += gridDim.x) {
+      const int kvh = w % a.n_kv_heads;
+      const int T0 = w / a.n_kv_heads * kQB;
+      const int T1 = min(T0 + kQB, rows);
+      if (is_v) {
+        // both Q tiles of the item, once every S product of the previous item has completed
         bool ok = true;
         if (lane == 0) {
-          const int s = i % depth;
-          const int round = i / depth;
-          ok = round == 0 || mbar_wait(&empty[s], (unsigned)((round - 1) & 1), a.err);
+          ok = nq == 0 || mbar_wait(q_empty, (unsigned)((nq - 1) & 1), a.err);
           if (ok) {
-            int ys[kUmSub], yo[kUmSub];
-            unsigned m = 0;
+            mbar_arrive_expect_tx(q_ready, 2 * Cfg::kQBytes);
 #pragma unroll
-            for (int sub = 0; sub < kUmSub; ++sub) {
-              const int k0 = tile * kUmKeys + sub * 16;
-              ys[sub] = -1;
-              yo[sub] = 0;
-              if (k0 < sg.kv_end) {
-                const int blk = __ldg(table + (k0 >> a.block_shift));
-                if (blk < 0 || blk >= a.num_blocks) {
-                  if (!is_v) raise_error(a.err, PA_DEVERR_BLOCK_ID);
-                } else {
-                  ys[sub] = blk;
-                  yo[sub] = k0 & bmask;
-                  m |= 1u << sub;
-                }
-              }
-            }
-            if (!is_v) {
-              // publish which sub-tiles hold data; the softmax groups read it instead of the table.
-              // Slot i % 8 was last read for tile i - 8, which both groups finished long ago: K tile
-              // i is loaded only after both S products of tile i - kUmKStages completed, which
-              // needed each group's P of tile i - kUmKStages - 1.
-              kmask[i & 7] = m;
-              mbar_arrive(&mready[i & 7]);
-            }
-            uint8_t* st = ring + s * Cfg::kKvBytes;
-            if (m == 0) {
-              mbar_arrive(&full[s]);
-            } else {
-              mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(m) * kHalves * 2048u);
+            for (int k = 0; k < 2; ++k)
 #pragma unroll
-              for (int sub = 0; sub < kUmSub; ++sub) {
-                if (ys[sub] < 0) continue;
-#pragma unroll
-                for (int h = 0; h < kHalves; ++h)
-                  tma_load_3d(st + h * Cfg::kKvHalf + sub * 2048, map, kvh * D + h * 64, yo[sub], ys[sub], &full[s]);
-              }
-            }
+              for (int h = 0; h < kHalves; ++h)
+                tma_load_3d(qs + k * Cfg::kQBytes + h * Cfg::kQHalf, &qmap, h * 64, kvh * G,
+                            T0 + k * (kUmTileRows / G), q_ready);
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -439,81 +409,167 @@ __global__ void __launch_bounds__(kUmThreads)
           alive = false;
           break;
         }
+        ++nq;
       }
-      t = sg.seg1;
+      for (int t = T0; t < T1 && alive;) {
+        const Seg sg = segment_at(t, T1);
+        const int32_t* table = a.block_table + (int64_t)sg.b * a.bt_stride;
+        const int nt = tiles_of(sg);
+        for (int tile = 0; tile < nt; ++tile, ++i) {
+          bool ok = true;
+          if (lane == 0) {
+            const int s = i % depth;
+            const int round = i / depth;
+            ok = round == 0 || mbar_wait(&empty[s], (unsigned)((round - 1) & 1), a.err);
+            if (ok) {
+              int ys[kUmSub], yo[kUmSub];
+              unsigned m = 0;
+#pragma unroll
+              for (int sub = 0; sub < kUmSub; ++sub) {
+                const int k0 = tile * kUmKeys + sub * 16;
+                ys[sub] = -1;
+                yo[sub] = 0;
+                if (k0 < sg.kv_end) {
+                  const int blk = __ldg(table + (k0 >> a.block_shift));
+                  if (blk < 0 || blk >= a.num_blocks) {
+                    if (!is_v) raise_error(a.err, PA_DEVERR_BLOCK_ID);
+                  } else {
+                    ys[sub] = blk;
+                    yo[sub] = k0 & bmask;
+                    m |= 1u << sub;
+                  }
+                }
+              }
+              if (!is_v) {
+                // publish which sub-tiles hold data; the softmax groups read it instead of the
+                // table.  Slot i % 8 was last read for tile i - 8, which both groups finished long
+                // ago: K tile i is loaded only after both S products of tile i - kUmKStages
+                // completed, which needed each group's P of tile i - kUmKStages - 1.
+                kmask[i & 7] = m;
+                mbar_arrive(&mready[i & 7]);
+              }
+              uint8_t* st = ring + s * Cfg::kKvBytes;
+              if (m == 0) {
+                mbar_arrive(&full[s]);
+              } else {
+                mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(m) * kHalves * 2048u);
+#pragma unroll
+                for (int sub = 0; sub < kUmSub; ++sub) {
+                  if (ys[sub] < 0) continue;
+#pragma unroll
+                  for (int h = 0; h < kHalves; ++h)
+                    tma_load_3d(st + h * Cfg::kKvHalf + sub * 2048, map, kvh * D + h * 64, yo[sub], ys[sub], &full[s]);
+                }
+              }
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+            alive = false;
+            break;
+          }
+        }
+        t = sg.seg1;
+      }
     }
     // Leave no copy in flight: after a normal run every issued tile was consumed and these waits
     // return at once; after a timeout elsewhere they wait (bounded) for this ring's last tiles.
     if (lane == 0) {
-      const int issued = i;  // a tile whose wait failed was not issued and not counted
-      for (int k = issued > depth ? issued - depth : 0; k < issued; ++k)
-        mbar_wait(&full[k % depth], (unsigned)((k / depth) & 1));
-      if (!is_v) mbar_wait(q_ready, 0);
+      for (int k = i > depth ? i - depth : 0; k < i; ++k) mbar_wait(&full[k % depth], (unsigned)((k / depth) & 1));
+      if (nq > 0) mbar_wait(q_ready, (unsigned)((nq - 1) & 1));
     }
   } else if (warp == 10) {
     // ------------------------------------------ MMA ---------------------------------------------
-    int n_all = 0;
-    for (int t = T0; t < T1;) {
-      const Seg sg = segment_at(t);
-      n_all += tiles_of(sg);
-      t = sg.seg1;
+    const uint32_t id_s = umma_idesc_f16(kBf16, 128, kUmKeys, false, false);
+    const uint32_t id_pv = umma_idesc_f16(kBf16, 128, D, false, true);
+    auto issue_s = [&](int k, int g) {
+      const uint32_t qa = smem_u32(qs + k * Cfg::kQBytes);
+      const uint32_t ka = smem_u32(ks + (g % kUmKStages) * Cfg::kKvBytes);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qo = (kk >> 2) * Cfg::kQHalf + (kk & 3) * 32;
+        const uint32_t ko = (kk >> 2) * Cfg::kKvHalf + (kk & 3) * 32;
+        umma_ss(tS(k), umma_desc_sw128(qa + qo, 16, 1024), umma_desc_sw128(ka + ko, 16, 1024), id_s,
+                kk > 0 ? 1u : 0u);
+      }
+      umma_commit(&s_full[k]);
+    };
+    auto issue_pv = [&](int k, int g, bool first) {
+      const uint32_t va = smem_u32(vs + (g % kUmVStages) * Cfg::kKvBytes);
+      // A = P_k from TMEM: 16 keys = 8 columns per instruction; an item's first tile starts O_k
+#pragma unroll
+      for (int kk = 0; kk < kUmKeys / 16; ++kk)
+        umma_ts(tO(k), tS(k) + 8u * (uint32_t)kk, umma_desc_sw128(va + kk * 2048, Cfg::kKvHalf, 1024), id_pv,
+                (!first || kk > 0) ? 1u : 0u);
+      umma_commit(&pv_done[k]);
+    };
+    int g = 0;  // tiles of earlier items
+    int n = 0;  // items done
+    bool alive = true;
+    for (int w = blockIdx.x; w < n_items && alive; w += gridDim.x, ++n) {
+      const int T0 = w / a.n_kv_heads * kQB;
+      const int T1 = min(T0 + kQB, rows);
+      int n_all = 0;
+      for (int t = T0; t < T1;) {
+        const Seg sg = segment_at(t, T1);
+        n_all += tiles_of(sg);
+        t = sg.seg1;
+      }
+      bool ok = true;
+      if (lane == 0) {
+        auto wait = [&](uint64_t* bar, unsigned parity) {
+          ok = ok && mbar_wait(bar, parity, a.err);
+          return ok;
+        };
+        // the item's first P V into O_k waits until group k has read O_k of the previous item
+        bool o_ready[2] = {n == 0, n == 0};
+        auto own_o = [&](int k) {
+          if (!o_ready[k]) {
+            o_ready[k] = true;
+            return wait(&o_free[k], (unsigned)((n - 1) & 1));
+          }
+          return ok;
+        };
+        // O_k += P_k V of item tile j; group 1's product closes the V tile
+        auto pv_of = [&](int k, int j) {
+          const int gj = g + j;
+          if (!own_o(k) || !wait(&p_full[k], (unsigned)(gj & 1)) ||
+              !wait(&vfull[gj % kUmVStages], (unsigned)((gj / kUmVStages) & 1)))
+            return false;
+          tc_fence_after();
+          issue_pv(k, gj, j == 0);
+          if (k == 1) umma_commit(&vempty[gj % kUmVStages]);
+          return true;
+        };
+        // Fixed issue order per tile: S_0(j), P_1(j-1) V, S_1(j), P_0(j) V.  While group 0 turns
+        // S_0(j) into P_0(j) the tensor core runs group 1's P V and next S, and the other way round.
+        // S_k overwrites the previous tile's P_k (also across items), so it waits for that P V.
+        wait(q_ready, (unsigned)(n & 1));
+        for (int j = 0; j < n_all && ok; ++j) {
+          const int gj = g + j;
+          if (!wait(&kfull[gj % kUmKStages], (unsigned)((gj / kUmKStages) & 1))) break;
+          if (gj > 0 && !wait(&pv_done[0], (unsigned)((gj - 1) & 1))) break;
+          tc_fence_after();
+          issue_s(0, gj);
+          if (j > 0 && !pv_of(1, j - 1)) break;
+          if (gj > 0 && !wait(&pv_done[1], (unsigned)((gj - 1) & 1))) break;
+          tc_fence_after();
+          issue_s(1, gj);
+          umma_commit(&kempty[gj % kUmKStages]);
+          if (j == n_all - 1) umma_commit(q_empty);  // after the item's last S products
+          if (!pv_of(0, j)) break;
+        }
+        if (ok && n_all > 0) pv_of(1, n_all - 1);
+        if (ok && n_all == 0) umma_commit(q_empty);
+        own_o(0);  // an item without tiles still takes its turn of both O buffers
+        own_o(1);
+      }
+      alive = __shfl_sync(0xffffffffu, ok, 0);
+      g += n_all;
     }
     if (lane == 0) {
-      const uint32_t id_s = umma_idesc_f16(kBf16, 128, kUmKeys, false, false);
-      const uint32_t id_pv = umma_idesc_f16(kBf16, 128, D, false, true);
-      auto issue_s = [&](int k, int i) {
-        const uint32_t qa = smem_u32(qs + k * Cfg::kQBytes);
-        const uint32_t ka = smem_u32(ks + (i % kUmKStages) * Cfg::kKvBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qo = (kk >> 2) * Cfg::kQHalf + (kk & 3) * 32;
-          const uint32_t ko = (kk >> 2) * Cfg::kKvHalf + (kk & 3) * 32;
-          umma_ss(tS(k), umma_desc_sw128(qa + qo, 16, 1024), umma_desc_sw128(ka + ko, 16, 1024), id_s,
-                  kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[k]);
-      };
-      auto issue_pv = [&](int k, int i) {
-        const uint32_t va = smem_u32(vs + (i % kUmVStages) * Cfg::kKvBytes);
-        // A = P_k from TMEM: 16 keys = 8 columns per instruction
-#pragma unroll
-        for (int kk = 0; kk < kUmKeys / 16; ++kk)
-          umma_ts(tO(k), tS(k) + 8u * (uint32_t)kk, umma_desc_sw128(va + kk * 2048, Cfg::kKvHalf, 1024), id_pv,
-                  (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&pv_done[k]);
-      };
-      // Fixed issue order per tile j: S_0(j), P_1(j-1) V, S_1(j), P_0(j) V.  While group 0 turns
-      // S_0(j) into P_0(j) the tensor core runs group 1's P V and next S, and the other way round.
-      // S_k(j) overwrites P_k(j-1), so it waits for O_k += P_k(j-1) V to complete.  The waits
-      // suspend the thread instead of polling, leaving issue slots to the softmax warps.
-      bool alive = mbar_wait(q_ready, 0, a.err);
-      auto wait = [&](uint64_t* bar, unsigned parity) {
-        alive = alive && mbar_wait(bar, parity, a.err);
-        return alive;
-      };
-      auto pv_of = [&](int k, int j) {  // O_k += P_k(j) V(j); group 1's closes V tile j
-        if (!wait(&p_full[k], (unsigned)(j & 1)) || !wait(&vfull[j % kUmVStages], (unsigned)((j / kUmVStages) & 1)))
-          return false;
-        tc_fence_after();
-        issue_pv(k, j);
-        if (k == 1) umma_commit(&vempty[j % kUmVStages]);
-        return true;
-      };
-      for (int j = 0; j < n_all && alive; ++j) {
-        if (!wait(&kfull[j % kUmKStages], (unsigned)((j / kUmKStages) & 1))) break;
-        if (j > 0 && !wait(&pv_done[0], (unsigned)((j - 1) & 1))) break;
-        tc_fence_after();
-        issue_s(0, j);
-        if (j > 0 && !pv_of(1, j - 1)) break;
-        if (j > 0 && !wait(&pv_done[1], (unsigned)((j - 1) & 1))) break;
-        tc_fence_after();
-        issue_s(1, j);
-        umma_commit(&kempty[j % kUmKStages]);
-        if (!pv_of(0, j)) break;
-      }
-      if (alive && n_all > 0) pv_of(1, n_all - 1);
       if (!alive) raise_error(a.err, PA_DEVERR_TIMEOUT);
-      if (n_all > 0) {
+      if (g > 0) {
         umma_commit(fin);
         mbar_wait(fin, 0, a.err);
       }
@@ -523,111 +579,121 @@ __global__ void __launch_bounds__(kUmThreads)
     const int grp = warp >> 2;           // 0 or 1
     const int r = threadIdx.x & 127;     // row inside the Q tile = TMEM lane
     const int row = grp * kUmTileRows + r;
-    const int tok = T0 + row / G;
-    const int head = kvh * G + row % G;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    float m_use = -INFINITY;  // stabilising maximum (log2 domain) the exponentials are taken against
-    float l_run = 0.f;
-    int i = 0;
+    int i = 0;  // tiles of this CTA so far
     bool alive = true;
-    for (int t = T0; t < T1 && alive;) {
-      const Seg sg = segment_at(t);
-      if (!sg.ok && threadIdx.x == 0) raise_error(a.err, PA_DEVERR_QUERY_LOC);
-      const int bound = (sg.ok && tok >= t && tok < sg.seg1) ? sg.pos0 + (tok - sg.q0) : -1;
-      const int nt = tiles_of(sg);
-      for (int tile = 0; tile < nt; ++tile, ++i) {
-        const int kb = tile * kUmKeys;
-        if (!__all_sync(0xffffffffu, mbar_wait(&mready[i & 7], (unsigned)((i >> 3) & 1), a.err))) {
-          alive = false;
-          break;
-        }
-        const unsigned loaded = kmask[i & 7];
-        // S_k of this tile is complete, and with it O_k += P_k V of the previous tile (issued before)
-        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], (unsigned)(i & 1), a.err))) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-        // tiles wholly inside every row's causal bound of the warp, with every sub-tile loaded, need
-        // no mask (the common case); the others mask per 32-key chunk
-        const float sc = a.scale_log2;
-        const unsigned all_sub = (1u << kUmSub) - 1u;
-        const bool unmasked = __all_sync(0xffffffffu, loaded == all_sub && kb + kUmKeys - 1 <= bound);
-        uint32_t mask[kUmKeys / 32];
-        {
-          const int lim = bound - kb;  // keys c <= lim are causal
-          const int nv = lim < 0 ? 0 : (lim >= kUmKeys ? kUmKeys : (int)lim + 1);
-#pragma unroll
-          for (int q = 0; q < kUmKeys / 32; ++q) {
-            const int lo = 32 * q;
-            const uint32_t cm = nv >= lo + 32 ? 0xFFFFFFFFu : (nv <= lo ? 0u : ((1u << (nv - lo)) - 1u));
-            const uint32_t lm = (((loaded >> (2 * q)) & 1u) ? 0x0000FFFFu : 0u) |
-                                (((loaded >> (2 * q + 1)) & 1u) ? 0xFFFF0000u : 0u);
-            mask[q] = cm & lm;
-          }
-        }
-        const uint32_t srow = tS(grp) + lane_base;
-        const float corr = (unmasked && sc >= 0.f) ? row_softmax<false, kBf16>(srow, sc, mask, m_use, l_run)
-                                                   : row_softmax<true, kBf16>(srow, sc, mask, m_use, l_run);
-        // O_k is stable here (its last product completed before this S_k was issued)
-        if (i > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32_sync(tO(grp) + lane_base + c0, v);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * corr);
-            tmem_st32(tO(grp) + lane_base + c0, v);
-          }
-        }
-        // group 0 zeroes V rows that hold no data or lie past the context (group 1's P V is issued
-        // after group 0's, so it sees the zeros too)
-        if (grp == 0 && (kb + kUmKeys > sg.n || loaded != all_sub)) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&vfull[i % kUmVStages], (unsigned)((i / kUmVStages) & 1), a.err))) {
+    for (int w = blockIdx.x; w < n_items && alive; w += gridDim.x) {
+      const int kvh = w % a.n_kv_heads;
+      const int T0 = w / a.n_kv_heads * kQB;
+      const int T1 = min(T0 + kQB, rows);
+      const int tok = T0 + row / G;
+      const int head = kvh * G + row % G;
+      const int i0 = i;
+      float m_use = -INFINITY;  // stabilising maximum (log2 domain) the exponentials are taken against
+      float l_run = 0.f;
+      for (int t = T0; t < T1 && alive;) {
+        const Seg sg = segment_at(t, T1);
+        if (!sg.ok && threadIdx.x == 0) raise_error(a.err, PA_DEVERR_QUERY_LOC);
+        const int bound = (sg.ok && tok >= t && tok < sg.seg1) ? sg.pos0 + (tok - sg.q0) : -1;
+        const int nt = tiles_of(sg);
+        for (int tile = 0; tile < nt; ++tile, ++i) {
+          const int kb = tile * kUmKeys;
+          if (!__all_sync(0xffffffffu, mbar_wait(&mready[i & 7], (unsigned)((i >> 3) & 1), a.err))) {
             alive = false;
             break;
           }
-          uint8_t* vst = vs + (i % kUmVStages) * Cfg::kKvBytes;
-          for (int e = r; e < kUmKeys * 8 * kHalves; e += 128) {
-            const int key = e / (8 * kHalves);
-            const int c = e % (8 * kHalves);
-            if (kb + key >= sg.n || !((loaded >> (key >> 4)) & 1u))
-              *reinterpret_cast<uint4*>(vst + sw_off(key, c, Cfg::kKvHalf)) = make_uint4(0, 0, 0, 0);
+          const unsigned loaded = kmask[i & 7];
+          // S_k of this tile is complete, and with it O_k += P_k V of the previous tile (issued before)
+          if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], (unsigned)(i & 1), a.err))) {
+            alive = false;
+            break;
           }
-          fence_proxy_async_smem();
+          tc_fence_after();
+          // tiles wholly inside every row's causal bound of the warp, with every sub-tile loaded,
+          // need no mask (the common case); the others mask per 32-key chunk
+          const float sc = a.scale_log2;
+          const unsigned all_sub = (1u << kUmSub) - 1u;
+          const bool unmasked = __all_sync(0xffffffffu, loaded == all_sub && kb + kUmKeys - 1 <= bound);
+          uint32_t mask[kUmKeys / 32];
+          {
+            const int lim = bound - kb;  // keys c <= lim are causal
+            const int nv = lim < 0 ? 0 : (lim >= kUmKeys ? kUmKeys : lim + 1);
+#pragma unroll
+            for (int q = 0; q < kUmKeys / 32; ++q) {
+              const int lo = 32 * q;
+              const uint32_t cm = nv >= lo + 32 ? 0xFFFFFFFFu : (nv <= lo ? 0u : ((1u << (nv - lo)) - 1u));
+              const uint32_t lm = (((loaded >> (2 * q)) & 1u) ? 0x0000FFFFu : 0u) |
+                                  (((loaded >> (2 * q + 1)) & 1u) ? 0xFFFF0000u : 0u);
+              mask[q] = cm & lm;
+            }
+          }
+          const uint32_t srow = tS(grp) + lane_base;
+          const float corr = (unmasked && sc >= 0.f) ? row_softmax<false, kBf16>(srow, sc, mask, m_use, l_run)
+                                                     : row_softmax<true, kBf16>(srow, sc, mask, m_use, l_run);
+          // O_k is stable here (its last product completed before this S_k was issued); the item's
+          // first tile starts O_k afresh, so only later tiles rescale it
+          if (i > i0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t v[32];
+              tmem_ld32_sync(tO(grp) + lane_base + c0, v);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * corr);
+              tmem_st32(tO(grp) + lane_base + c0, v);
+            }
+          }
+          // group 0 zeroes V rows that hold no data or lie past the context (group 1's P V is issued
+          // after group 0's, so it sees the zeros too)
+          if (grp == 0 && (kb + kUmKeys > sg.n || loaded != all_sub)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&vfull[i % kUmVStages], (unsigned)((i / kUmVStages) & 1), a.err))) {
+              alive = false;
+              break;
+            }
+            uint8_t* vst = vs + (i % kUmVStages) * Cfg::kKvBytes;
+            for (int e = r; e < kUmKeys * 8 * kHalves; e += 128) {
+              const int key = e / (8 * kHalves);
+              const int c = e % (8 * kHalves);
+              if (kb + key >= sg.n || !((loaded >> (key >> 4)) & 1u))
+                *reinterpret_cast<uint4*>(vst + sw_off(key, c, Cfg::kKvHalf)) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&p_full[grp]);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&p_full[grp]);
+        t = sg.seg1;
       }
-      t = sg.seg1;
-    }
-    if (!alive && lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
-    if (alive && i > 0) {
-      alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[grp], (unsigned)((i - 1) & 1), a.err));
-      tc_fence_after();
-    }
-    const bool have = alive && i > 0 && l_run != 0.f;
-    const float inv = have ? 1.f / l_run : 0.f;
-    T* orow = static_cast<T*>(a.out) + ((int64_t)tok * a.n_q_heads + head) * D;
+      if (!alive && lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+      if (alive && i > i0) {
+        alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[grp], (unsigned)((i - 1) & 1), a.err));
+        tc_fence_after();
+      }
+      const bool have = alive && i > i0 && l_run != 0.f;
+      const float inv = have ? 1.f / l_run : 0.f;
+      T* orow = static_cast<T*>(a.out) + ((int64_t)tok * a.n_q_heads + head) * D;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t v[32];
-      tmem_ld32_sync(tO(grp) + lane_base + c0, v);
-      if (tok < T1) {
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32_sync(tO(grp) + lane_base + c0, v);
+        if (tok < T1) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          float f[8];
+          for (int j = 0; j < 32; j += 8) {
+            float f[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = have ? __uint_as_float(v[j + e]) * inv : 0.f;
-          uint4 w;
-          w.x = pack2<kBf16>(f[0], f[1]);
-          w.y = pack2<kBf16>(f[2], f[3]);
-          w.z = pack2<kBf16>(f[4], f[5]);
-          w.w = pack2<kBf16>(f[6], f[7]);
-          *reinterpret_cast<uint4*>(orow + c0 + j) = w;
+            for (int e = 0; e < 8; ++e) f[e] = have ? __uint_as_float(v[j + e]) * inv : 0.f;
+            uint4 wv;
+            wv.x = pack2<kBf16>(f[0], f[1]);
+            wv.y = pack2<kBf16>(f[2], f[3]);
+            wv.z = pack2<kBf16>(f[4], f[5]);
+            wv.w = pack2<kBf16>(f[6], f[7]);
+            *reinterpret_cast<uint4*>(orow + c0 + j) = wv;
+          }
         }
       }
+      // O_k has been read: the next item's first P V may overwrite it
+      tc_fence_before();
+      mbar_arrive(&o_free[grp]);
     }
   }
   tc_fence_before();
@@ -658,9 +724,18 @@ static cudaError_t launch_um_g(const AttnArgs& a, const CUtensorMap& km, const C
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   constexpr int qb = kUmRows / G;
-  const int64_t grid = ((a.rows + qb - 1) / qb) * a.n_kv_heads;
-  if (grid <= 0) return cudaSuccess;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int64_t items = ((a.rows + qb - 1) / qb) * a.n_kv_heads;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // persistent: one CTA per SM walks the work items, so the next item's loads overlap this one's end
+  static int sm_count[64] = {};
+  int sms = dev >= 0 && dev < 64 ? sm_count[dev] : 0;
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) sm_count[dev] = sms;
+  }
+  const int64_t grid = kUmPersistent ? std::min<int64_t>(items, sms) : items;
   prefill_umma_kernel<T, D, G><<<(unsigned)grid, kUmThreads, smem, s>>>(a, km, vm, qm);
   return cudaGetLastError();
 }
