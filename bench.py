@@ -36,9 +36,10 @@ HQ, HKV, D, S = 32, 8, 128, 16
 LLAMA_LAYERS = 32
 ELT = 2  # bf16
 # dram__bytes_read.sum + dram__bytes_write.sum of one paged_attention_decode_fused call on this
-# workload with separate pools (partition kernel 578.8 + 3.8 MB, merge kernel 2.5 MB; mean of two
-# calls), from one ncu capture of those three metrics.  Retake it whenever either kernel changes.
-FUSED_CALL_DRAM_BYTES = 585.1e6
+# workload with separate pools and the per-partition grid (partition kernel 578.7 + 3.6 MB, merge
+# kernel 2.5 MB; mean of two calls), from one ncu capture of those three metrics.  Retake it whenever
+# either kernel changes.
+FUSED_CALL_DRAM_BYTES = 584.9e6
 
 
 def measured_peaks():
@@ -387,6 +388,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--partition-tokens", type=int, default=0, help="split-K partition length (0 = library default)")
     ap.add_argument("--decode-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--decode-grid", type=int, default=0,
+                    help="split-K grid of the tensor-core decode: 0 one CTA per partition, 1 equal work per warp")
     ap.add_argument("--workload", choices=["decode", "prefill", "swap"], default="decode")
     ap.add_argument("--unfused", action="store_true",
                     help="time paged_kv_write + paged_attention_decode as two calls instead of the fused call")
@@ -408,6 +411,7 @@ def main():
     lib = pa.load_library()
     pa.set_option(pa.PA_OPT_PARTITION_TOKENS, args.partition_tokens)
     pa.set_option(pa.PA_OPT_DECODE_KERNEL, args.decode_kernel)
+    pa.set_option(pa.PA_OPT_DECODE_GRID, args.decode_grid)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
@@ -595,6 +599,7 @@ def main():
                    "parallelism": f"replicas x{world}",
                    "partition_tokens": args.partition_tokens or 1024,
                    "decode_kernel": ["auto", "cuda-core", "tensor-core"][args.decode_kernel],
+                   "decode_grid": ["one CTA per partition", "equal work per warp"][args.decode_grid],
                    "kv_layout": args.kv_layout},
         "pct_hbm_measured": value / peak,
         "pct_hbm_spec_8000": value / 8000.0,
@@ -607,7 +612,8 @@ def main():
                      "frac": achieved / peak,
                      # DRAM bytes of one fused call (both kernels) from the ncu capture; None for the
                      # two-call variant and for the unified layout (not captured)
-                     "traffic": FUSED_CALL_DRAM_BYTES if use_fused and args.kv_layout == "separate" else None},
+                     "traffic": (FUSED_CALL_DRAM_BYTES if use_fused and args.kv_layout == "separate"
+                                 and args.decode_grid == 0 else None)},
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,

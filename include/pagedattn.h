@@ -100,8 +100,14 @@ enum {
                                   memory) instead of the workspace + merge kernel.  Off by default: a
                                   cluster keeps all its CTAs resident until its longest partition ends,
                                   which cost 20 % at the serving shape */
-  PA_OPT_KV_LAYOUT = 6         /* pool layout of every call: 0 (default) separate K and V pools (see
+  PA_OPT_KV_LAYOUT = 6,        /* pool layout of every call: 0 (default) separate K and V pools (see
                                   "Pools"); 1 unified K/V blocks (see "Unified K/V blocks") */
+  PA_OPT_DECODE_GRID = 7       /* split-K grid of the tensor-core decode when rows split: 0 (default)
+                                  one CTA per (sequence, KV head, partition_tokens-long partition),
+                                  scheduled by the hardware; 1 equal work per warp (each KV head's
+                                  tiles of all sequences laid end to end and cut into one wave of
+                                  equal ranges).  Measured slower at the serving shape: a static
+                                  split cannot follow the uneven bandwidth the SMs get */
 };
 
 /*

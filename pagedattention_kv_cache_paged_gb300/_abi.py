@@ -22,7 +22,7 @@ _DTYPE_CODES = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16, torch.float32: 
 
 PA_OK, PA_EINVAL, PA_EDTYPE, PA_ERANGE, PA_EWORKSPACE, PA_ECUDA, PA_EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 PA_OPT_CHECKED, PA_OPT_DECODE_KERNEL, PA_OPT_PARTITION_TOKENS, PA_OPT_PREFILL_KERNEL = 1, 2, 3, 4
-PA_OPT_CLUSTER_MERGE, PA_OPT_KV_LAYOUT = 5, 6
+PA_OPT_CLUSTER_MERGE, PA_OPT_KV_LAYOUT, PA_OPT_DECODE_GRID = 5, 6, 7
 KV_LAYOUT_SEPARATE, KV_LAYOUT_UNIFIED = 0, 1
 PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT, PA_DEVERR_CONTEXT_LEN = 1, 2, 4
 PA_DEVERR_COPY_PAIR, PA_DEVERR_QUERY_LOC, PA_DEVERR_TIMEOUT = 8, 16, 32

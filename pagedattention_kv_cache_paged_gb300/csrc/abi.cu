@@ -135,16 +135,24 @@ void plan_split(int64_t bt_stride, int block_size, int* part_tokens, int* max_pa
 
 struct WsLayout {
   size_t bytes;
-  size_t off_m, off_l;
+  size_t off_m, off_l, off_np;
+  int slots;  // split-K slots per (sequence, query head) row
 };
 
-WsLayout workspace_layout(int64_t rows_heads, int max_parts, int head_dim) {
+// Split-K workspace when rows split into up to max_parts partitions: acc[rows_heads][slots][head_dim],
+// then m[rows_heads][slots], l[rows_heads][slots], np[batch] (int32), each section 16-byte aligned.
+// slots = max_parts + 1: the per-partition grid uses the first max_parts of each row; the equal-work
+// grid makes its ranges long enough that no sequence meets more than slots of them.
+WsLayout workspace_layout(int batch, int64_t rows_heads, int max_parts, int head_dim) {
   WsLayout w{};
   if (max_parts <= 1) return w;
-  const size_t n = (size_t)rows_heads * (size_t)max_parts;
+  w.slots = max_parts + 1;
+  const size_t n = (size_t)rows_heads * (size_t)w.slots;
+  auto up16 = [](size_t x) { return (x + 15) & ~size_t(15); };
   w.off_m = n * (size_t)head_dim * sizeof(float);
-  w.off_l = w.off_m + ((n * sizeof(float) + 15) & ~size_t(15));
-  w.bytes = w.off_l + ((n * sizeof(float) + 15) & ~size_t(15));
+  w.off_l = w.off_m + up16(n * sizeof(float));
+  w.off_np = w.off_l + up16(n * sizeof(float));
+  w.bytes = w.off_np + up16((size_t)batch * sizeof(int32_t));
   return w;
 }
 
@@ -171,6 +179,7 @@ int pa_set_option(int option, int64_t value) {
       break;
     case PA_OPT_CLUSTER_MERGE:
     case PA_OPT_KV_LAYOUT:
+    case PA_OPT_DECODE_GRID:
       if (value != 0 && value != 1) return PA_EINVAL;
       break;
     default:
@@ -181,7 +190,7 @@ int pa_set_option(int option, int64_t value) {
 }
 
 int64_t pa_get_option(int option) {
-  if (option < 1 || option > 6) return PA_EINVAL;
+  if (option < 1 || option > 7) return PA_EINVAL;
   return g_options[option].load();
 }
 
@@ -259,7 +268,7 @@ size_t paged_attention_decode_workspace_size(int batch, int64_t block_table_stri
   if (batch <= 0 || block_table_stride <= 0 || block_size <= 0 || n_q_heads <= 0 || head_dim <= 0) return 0;
   int part = 0, max_parts = 1;
   plan_split(block_table_stride, block_size, &part, &max_parts);
-  return workspace_layout((int64_t)batch * n_q_heads, max_parts, head_dim).bytes;
+  return workspace_layout(batch, (int64_t)batch * n_q_heads, max_parts, head_dim).bytes;
 }
 
 static int decode_impl(void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -315,7 +324,7 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
 
   int part_tokens = 0, max_parts = 1;
   plan_split(block_table_stride, block_size, &part_tokens, &max_parts);
-  WsLayout ws = workspace_layout((int64_t)batch * n_q_heads, max_parts, head_dim);
+  WsLayout ws = workspace_layout(batch, (int64_t)batch * n_q_heads, max_parts, head_dim);
   // up to 8 partitions per row on the tensor-core path: one thread-block cluster per row merges
   // through distributed shared memory, with neither workspace nor merge kernel
   const bool cluster = use_tc && max_parts >= 2 && max_parts <= 8 && g_options[PA_OPT_CLUSTER_MERGE].load() != 0;
@@ -349,11 +358,17 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
   a.head_dim = head_dim;
   a.part_tokens = part_tokens;
   a.max_parts = max_parts;
+  // equal-work grid on the tensor-core path when rows split and PA_OPT_DECODE_GRID is 1
+  const bool balanced = use_tc && max_parts > 1 && !cluster && g_options[PA_OPT_DECODE_GRID].load() == 1;
   if (max_parts > 1 && !cluster) {
     char* base = static_cast<char*>(workspace);
     a.ws_acc = reinterpret_cast<float*>(base);
     a.ws_m = reinterpret_cast<float*>(base + ws.off_m);
     a.ws_l = reinterpret_cast<float*>(base + ws.off_l);
+    if (balanced) {
+      a.ws_np = reinterpret_cast<int32_t*>(base + ws.off_np);
+      a.max_parts = ws.slots;
+    }
   }
   a.cluster = cluster ? 1 : 0;
   a.err = err;
@@ -365,7 +380,9 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
     a.v_pool_w = const_cast<void*>(v_pool);
   }
   int launches = 0;
-  cudaError_t e = use_tc ? launch_decode_tc(a, dtype, s, &launches) : launch_attn_simt(a, dtype, s, &launches);
+  cudaError_t e = balanced ? launch_decode_bal(a, dtype, s, &launches)
+                 : use_tc ? launch_decode_tc(a, dtype, s, &launches)
+                          : launch_attn_simt(a, dtype, s, &launches);
   if (e == cudaSuccess && max_parts > 1 && !cluster) {
     MergeArgs m{};
     m.out = out;
@@ -373,7 +390,8 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
     m.part_l = a.ws_l;
     m.part_acc = a.ws_acc;
     m.rows = (int64_t)batch * n_q_heads;
-    m.n_parts = max_parts;
+    m.n_parts = a.max_parts;
+    m.seq_parts = a.ws_np;
     m.head_dim = head_dim;
     m.context_lens = context_lens;
     m.heads_per_seq = n_q_heads;

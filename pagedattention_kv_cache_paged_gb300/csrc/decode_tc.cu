@@ -49,6 +49,10 @@ namespace pa {
 #ifndef PA_TC_MIN_CTAS
 #define PA_TC_MIN_CTAS 3
 #endif
+// 1: decode grids are launched with programmatic dependent launch (see launch_tc_g)
+#ifndef PA_DECODE_PDL
+#define PA_DECODE_PDL 1
+#endif
 
 constexpr int kTcWarps = PA_TC_WARPS;
 constexpr int kTile = 16;          // tokens per tile (one mma k-step of PV)
@@ -65,11 +69,131 @@ struct TcCfg {
   static_assert(kTcWarps * kStages * 8 <= 1024, "barriers must fit their 1 KB slot");
 };
 
+// Q fragments of the mma A operand for the query group of KV head kvh in sequence b: rows = query
+// heads, two b32 (4 elements) per k-step per lane; rows >= G are zero.
+template <typename T, int D, int G>
+__device__ __forceinline__ void load_q_frags(const AttnArgs& a, int64_t b, int kvh, int lane,
+                                             uint32_t (&qa)[D / 16][2]) {
+  const int g = lane >> 2, tig = lane & 3;
+  const T* qrow = static_cast<const T*>(a.q) + (b * a.n_q_heads + (int64_t)kvh * G + g) * D;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    if (g < G) {
+      qa[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig));
+      qa[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig));
+    } else {
+      qa[ks][0] = 0u;
+      qa[ks][1] = 0u;
+    }
+  }
+}
+
+// This step's token of KV head kvh, row r of the 16-token tile at st: from k_src / v_src (head_dim
+// elements each) into shared memory, swizzled like the TMA boxes, and into the pools at k_dst / v_dst.
+template <typename T, int D>
+__device__ __forceinline__ void patch_new_token(uint8_t* st, int r, const T* k_src, const T* v_src, T* k_dst,
+                                                T* v_dst, int lane) {
+  constexpr int kHalves = D / 64;
+  constexpr int kChunks = D / 8;
+  if (lane < 2 * kChunks) {
+    const bool isv = lane >= kChunks;
+    const int c = lane % kChunks;
+    const uint4 val = __ldg(reinterpret_cast<const uint4*>((isv ? v_src : k_src) + c * 8));
+    *reinterpret_cast<uint4*>(st + ((isv ? kHalves : 0) + (c >> 3)) * kHalfBytes + r * 128 +
+                              (((c & 7) ^ (r & 7)) << 4)) = val;
+    *reinterpret_cast<uint4*>((isv ? v_dst : k_dst) + c * 8) = val;
+  }
+  __syncwarp();
+}
+
+// Folds one 16-token K/V tile (at st, in the swizzled TMA layout) into the warp's online-softmax
+// state (o, m_run, l_run; rows = query heads in the mma layout).  Tokens >= valid are masked and
+// their V rows zeroed first.
+template <typename T, int D>
+__device__ __forceinline__ void tile_update(uint8_t* st, int valid, const uint32_t (&qa)[D / 16][2],
+                                            float (&o)[D / 8][4], float& m_run, float& l_run, float scale_log2,
+                                            int lane) {
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  constexpr int kHalves = D / 64;
+  constexpr int kKSteps = D / 16;
+  constexpr int kDTiles = D / 8;
+  const int tig = lane & 3;
+  const uint32_t k_base = smem_u32(st);
+  const uint32_t v_base = smem_u32(st + kHalves * kHalfBytes);
+  if (valid < kTile) {
+    // zero the V rows past the end (both halves): 16-byte stores, rows valid..15
+    const int nz = (kTile - valid) * 8 * kHalves;
+    for (int i = lane; i < nz; i += 32) {
+      const int h = i / ((kTile - valid) * 8);
+      const int r = valid + (i / 8) % (kTile - valid);
+      const int c = i % 8;
+      *reinterpret_cast<uint4*>(st + (kHalves + h) * kHalfBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+  }
+  // ---- S = Q K^T: two n-tiles of 8 tokens ------------------------------------------------------
+  float sc[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    const int tok = nt * 8 + (lane & 7);
+#pragma unroll
+    for (int ks = 0; ks < kKSteps; ks += 2) {
+      const int chunk = 2 * ks + (lane >> 3);  // 8-element chunk along head_dim
+      const uint32_t addr = k_base + (chunk >> 3) * kHalfBytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(addr, b0, b1, b2, b3);
+      mma_16816<kBf16>(sc[nt], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+      mma_16816<kBf16>(sc[nt], qa[ks + 1][0], 0u, qa[ks + 1][1], 0u, b2, b3);
+    }
+  }
+  // ---- online softmax over the tile (rows g, columns = tokens) -----------------------------------
+  float x[4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int tok = nt * 8 + 2 * tig + e;
+      x[nt * 2 + e] = tok < valid ? sc[nt][e] * scale_log2 : -INFINITY;
+    }
+  }
+  float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+  tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+  const float m_new = fmaxf(m_run, tmax);
+  const float corr = fast_exp2(m_run - m_new);
+  float p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - m_new);
+  l_run = l_run * corr + ((p[0] + p[1]) + (p[2] + p[3]));
+  if (__any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+    for (int i = 0; i < kDTiles; ++i) {
+      o[i][0] *= corr;
+      o[i][1] *= corr;
+    }
+  }
+  m_run = m_new;
+  // ---- O += P V: P from the score registers, V^T fragments by ldmatrix.trans ---------------------
+  const uint32_t pa0 = pack2<kBf16>(p[0], p[1]);
+  const uint32_t pa2 = pack2<kBf16>(p[2], p[3]);
+#pragma unroll
+  for (int dt = 0; dt < kDTiles; dt += 2) {
+    const int mi = lane >> 3;
+    const int tok = (lane & 7) + 8 * (mi & 1);
+    const int chunk = dt + (mi >> 1);
+    const uint32_t addr = v_base + (chunk >> 3) * kHalfBytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4_t(addr, b0, b1, b2, b3);
+    mma_16816<kBf16>(o[dt], pa0, 0u, pa2, 0u, b0, b1);
+    mma_16816<kBf16>(o[dt + 1], pa0, 0u, pa2, 0u, b2, b3);
+  }
+}
+
 template <typename T, int D, int G, bool kCluster>
 __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
     decode_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
-  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr int kHalves = TcCfg<D>::kHalves;
   constexpr int kStageBytes = TcCfg<D>::kStageBytes;
   constexpr int kStages = TcCfg<D>::kStages;
@@ -93,6 +217,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   const int g = lane >> 2;   // mma row group: query head g of the group
   const int tig = lane & 3;  // thread in group
 
+  // launched with programmatic serialization: wait for the preceding grid (its outputs may be this
+  // call's inputs, and its reads of out / workspace must end before this grid writes them)
+  pdl_wait_primary();
   const int64_t max_len = a.bt_stride << a.block_shift;
   const int b = (int)row;
   int64_t len = __ldg(a.context_lens + b);
@@ -168,21 +295,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
     for (int j = 0; j < pre; ++j) issue(j);
   }
 
-  // Q fragments of the A operand: rows = query heads, two b32 (4 elements) per k-step per lane.
   uint32_t qa[kKSteps][2];
-  {
-    const T* qrow = static_cast<const T*>(a.q) + (row * a.n_q_heads + (int64_t)kvh * G + g) * D;
-#pragma unroll
-    for (int ks = 0; ks < kKSteps; ++ks) {
-      if (g < G) {
-        qa[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig));
-        qa[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig));
-      } else {
-        qa[ks][0] = 0u;
-        qa[ks][1] = 0u;
-      }
-    }
-  }
+  load_q_frags<T, D, G>(a, row, kvh, lane, qa);
 
   float o[kDTiles][4];
 #pragma unroll
@@ -190,111 +304,42 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   float m_run = -INFINITY, l_run = 0.f;
   bool timed_out = false;
 
+  int j_fail = my_tiles;  // first tile whose wait gave up
   for (int j = 0; j < my_tiles; ++j) {
     const int s = j % kStages;
-    if (!mbar_wait(&my_bars[s], (unsigned)((j / kStages) & 1), a.err)) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&my_bars[s], (unsigned)((j / kStages) & 1), a.err))) {
       timed_out = true;
+      j_fail = j;
       break;
     }
     const int blk = tile_block(j);
     const int64_t t0 = tile_t0(j);
     const int valid = (int)(t_end - t0 < kTile ? t_end - t0 : kTile);
     uint8_t* st = my_stages + s * kStageBytes;
-    const uint32_t k_base = smem_u32(st);
-    const uint32_t v_base = smem_u32(st + kHalves * kHalfBytes);
     if (blk >= 0 && blk < a.num_blocks) {
       if (warp + kTcWarps * j == patch_tile) {
         // this step's token: row (len - 1) mod 16 of the tile, from k_new / v_new, into shared
-        // memory (swizzled like the TMA boxes) and into the pool
-        constexpr int kChunks = D / 8;
-        const int r = (int)((len - 1) & (kTile - 1));
-        if (lane < 2 * kChunks) {
-          const bool isv = lane >= kChunks;
-          const int c = lane % kChunks;
-          const int64_t src_off = ((int64_t)b * a.n_kv_heads + kvh) * D + c * 8;
-          const uint4 val = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(isv ? a.v_new : a.k_new) + src_off));
-          *reinterpret_cast<uint4*>(st + ((isv ? kHalves : 0) + (c >> 3)) * kHalfBytes + r * 128 +
-                                    (((c & 7) ^ (r & 7)) << 4)) = val;
-          T* dst = static_cast<T*>(isv ? a.v_pool_w : a.k_pool_w) + new_row + (int64_t)kvh * D + c * 8;
-          *reinterpret_cast<uint4*>(dst) = val;
-        }
-        __syncwarp();
+        // memory and into the pool
+        const int64_t src_off = ((int64_t)b * a.n_kv_heads + kvh) * D;
+        const int64_t dst_off = new_row + (int64_t)kvh * D;
+        patch_new_token<T, D>(st, (int)((len - 1) & (kTile - 1)), static_cast<const T*>(a.k_new) + src_off,
+                              static_cast<const T*>(a.v_new) + src_off, static_cast<T*>(a.k_pool_w) + dst_off,
+                              static_cast<T*>(a.v_pool_w) + dst_off, lane);
       }
-      if (valid < kTile) {
-        // zero the V rows past the end (both halves): 16-byte stores, rows valid..15
-        const int nz = (kTile - valid) * 8 * kHalves;
-        for (int i = lane; i < nz; i += 32) {
-          const int h = i / ((kTile - valid) * 8);
-          const int r = valid + (i / 8) % (kTile - valid);
-          const int c = i % 8;
-          *reinterpret_cast<uint4*>(st + (kHalves + h) * kHalfBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-        }
-        __syncwarp();
-      }
-      // ---- S = Q K^T: two n-tiles of 8 tokens ----------------------------------------------
-      float sc[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-        const int tok = nt * 8 + (lane & 7);
-#pragma unroll
-        for (int ks = 0; ks < kKSteps; ks += 2) {
-          const int chunk = 2 * ks + (lane >> 3);  // 8-element chunk along head_dim
-          const uint32_t addr = k_base + (chunk >> 3) * kHalfBytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(addr, b0, b1, b2, b3);
-          mma_16816<kBf16>(sc[nt], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
-          mma_16816<kBf16>(sc[nt], qa[ks + 1][0], 0u, qa[ks + 1][1], 0u, b2, b3);
-        }
-      }
-      // ---- online softmax over the tile (rows g, columns = tokens) ---------------------------
-      float x[4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int tok = nt * 8 + 2 * tig + e;
-          x[nt * 2 + e] = tok < valid ? sc[nt][e] * a.scale_log2 : -INFINITY;
-        }
-      }
-      float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-      const float m_new = fmaxf(m_run, tmax);
-      const float corr = fast_exp2(m_run - m_new);
-      float p[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - m_new);
-      l_run = l_run * corr + ((p[0] + p[1]) + (p[2] + p[3]));
-      if (__any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll
-        for (int i = 0; i < kDTiles; ++i) {
-          o[i][0] *= corr;
-          o[i][1] *= corr;
-        }
-      }
-      m_run = m_new;
-      // ---- O += P V: P from the score registers, V^T fragments by ldmatrix.trans ----------------
-      const uint32_t pa0 = pack2<kBf16>(p[0], p[1]);
-      const uint32_t pa2 = pack2<kBf16>(p[2], p[3]);
-#pragma unroll
-      for (int dt = 0; dt < kDTiles; dt += 2) {
-        const int mi = lane >> 3;
-        const int tok = (lane & 7) + 8 * (mi & 1);
-        const int chunk = dt + (mi >> 1);
-        const uint32_t addr = v_base + (chunk >> 3) * kHalfBytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(addr, b0, b1, b2, b3);
-        mma_16816<kBf16>(o[dt], pa0, 0u, pa2, 0u, b0, b1);
-        mma_16816<kBf16>(o[dt + 1], pa0, 0u, pa2, 0u, b2, b3);
-      }
+      tile_update<T, D>(st, valid, qa, o, m_run, l_run, a.scale_log2, lane);
     }
     // release the stage and refill it with this warp's tile j + kStages
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0 && j + kStages < my_tiles) issue(j + kStages);
   }
-  if (timed_out && lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+  if (timed_out && lane == 0) {
+    raise_error(a.err, PA_DEVERR_TIMEOUT);
+    // leave no copy in flight: wait (bounded) for the tiles issued from j_fail on
+    const int issued = j_fail + kStages < my_tiles ? j_fail + kStages : my_tiles;
+    for (int j = j_fail; j < issued; ++j) mbar_wait(&my_bars[j % kStages], (unsigned)((j / kStages) & 1));
+  }
+  __syncwarp();
 
   // ---- combine: quad-reduce l, stage (m, l, o) per warp in the warp's own stage 0 --------------
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
@@ -393,6 +438,255 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
 }
 
 // ------------------------------------------------------------------------------------------------
+// Equal-work grid.  Per KV head, the 16-token tiles of all sequences are laid end to end
+// (sequence 0's tiles, then sequence 1's, ...) and cut into n_units = n_ctas x kTcWarps ranges of
+// `per` consecutive tiles; warp w of CTA (c, kvh) streams range c * kTcWarps + w through its own
+// TMA ring.  per = max(ceil(total / n_units), ceil(t_max / (slots - 1))), t_max the longest
+// sequence's tile count and slots = a.max_parts the split-K slots per row, so that no sequence
+// meets more ranges than it has slots.  The grid is one wave
+// (n_ctas x n_kv_heads CTAs resident at once), so every warp streams the same number of bytes,
+// none waits for another (there is no barrier in the kernel) and none waits for a straggler CTA;
+// the warps of one range index (one per KV head) read the same physical blocks at the same time.
+// A range meets a sequence in one segment.  At each segment end the warp writes the output (a
+// sequence inside one range) or the segment's partial state into the sequence's split-K slot
+// q - q_first(b), where q is the range and q_first(b) the range holding the sequence's first tile;
+// the warp holding that first tile also records the sequence's number of slots for the merge
+// kernel.  A sequence of t tiles meets at most ceil(t / per) + 1 <= slots ranges.
+// ------------------------------------------------------------------------------------------------
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
+    decode_bal_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap) {
+  constexpr int kHalves = TcCfg<D>::kHalves;
+  constexpr int kStageBytes = TcCfg<D>::kStageBytes;
+  constexpr int kStages = TcCfg<D>::kStages;
+  constexpr int kKSteps = D / 16;
+  constexpr int kDTiles = D / 8;
+  static_assert(G <= 8, "query group must fit the first 8 rows of the mma tile");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base);
+  uint8_t* stages = base + 1024;
+
+  const int kvh = (int)(blockIdx.x % a.n_kv_heads);
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int q_unit = (int)(blockIdx.x / a.n_kv_heads) * kTcWarps + warp;  // this warp's range
+  const int n_units = (int)(gridDim.x / a.n_kv_heads) * kTcWarps;
+  const int g = lane >> 2;
+  const int tig = lane & 3;
+  const int64_t max_len = a.bt_stride << a.block_shift;
+  const int bmask = a.block_size - 1;
+
+  auto len_of = [&](int b) -> int64_t {
+    const int64_t n = __ldg(a.context_lens + b);
+    return n < 0 ? 0 : (n > max_len ? max_len : n);
+  };
+  auto tiles_of = [&](int b) -> int64_t { return (len_of(b) + kTile - 1) / kTile; };
+
+  pdl_wait_primary();       // the preceding grid has completed (see decode_tc_kernel)
+  pdl_launch_dependents();  // the split-K merge may begin launching; it waits for this grid's results
+
+  // ---- this warp's range [r0, r1) of the concatenated tiles --------------------------------------
+  int64_t total = 0, t_max = 0;
+  for (int b0 = 0; b0 < a.batch; b0 += 32) {
+    const int b = b0 + lane;
+    int64_t t = 0;
+    if (b < a.batch) {
+      const int64_t n = __ldg(a.context_lens + b);
+      if ((n < 0 || n > max_len) && blockIdx.x == 0 && warp == 0) raise_error(a.err, PA_DEVERR_CONTEXT_LEN);
+      t = tiles_of(b);
+    }
+    int64_t tm = t;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      t += __shfl_xor_sync(0xffffffffu, t, off);
+      tm = max(tm, __shfl_xor_sync(0xffffffffu, tm, off));
+    }
+    total += t;
+    t_max = max(t_max, tm);
+  }
+  const int64_t per_slots = (t_max + a.max_parts - 2) / (a.max_parts - 1);  // ceil(t_max / (slots - 1))
+  const int64_t per = max(max((total + n_units - 1) / n_units, per_slots), (int64_t)1);
+  const int64_t r0 = (int64_t)q_unit * per;
+  if (r0 >= total) return;  // nothing left for this range (no barrier follows in this kernel)
+  const int64_t r1 = min(r0 + per, total);
+  const int my_tiles = (int)(r1 - r0);
+  // first sequence with a tile in the range: the smallest b with o_b + t_b > r0
+  int b_first = 0;
+  int64_t o_first = 0;
+  {
+    int64_t run = 0;
+    for (int b0 = 0; b0 < a.batch; b0 += 32) {
+      const int b = b0 + lane;
+      const int64_t t = b < a.batch ? tiles_of(b) : 0;
+      int64_t incl = t;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, b < a.batch && run + incl > r0);
+      if (hit != 0u) {
+        const int l = __ffs(hit) - 1;
+        b_first = b0 + l;
+        o_first = run + __shfl_sync(0xffffffffu, incl - t, l);
+        break;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+
+  uint64_t* my_bars = bars + warp * kStages;
+  uint8_t* my_stages = stages + warp * kStages * kStageBytes;
+  if (lane == 0) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+    for (int s = 0; s < kStages; ++s) mbar_init(&my_bars[s], 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+
+  // producer cursor (lane 0): sequence pb holds the next tile to issue; its tiles start at pob
+  int pb = b_first;
+  int64_t pob = o_first, pnt = tiles_of(b_first);
+  int issued = 0;
+  auto issue = [&](int k) {  // lane 0 only: the range's k-th tile
+    const int64_t u = r0 + k;
+    while (pob + pnt <= u) {
+      pob += pnt;
+      ++pb;
+      pnt = tiles_of(pb);
+    }
+    const int64_t t0 = (u - pob) * kTile;
+    const int blk = __ldg(a.block_table + (int64_t)pb * a.bt_stride + (t0 >> a.block_shift));
+    const int s = k % kStages;
+    ++issued;
+    if (blk < 0 || blk >= a.num_blocks) {
+      raise_error(a.err, PA_DEVERR_BLOCK_ID);
+      mbar_arrive(&my_bars[s]);  // complete the phase without data; the consumer skips the tile
+      return;
+    }
+    const int off = (int)(t0 & bmask);
+    uint8_t* st = my_stages + s * kStageBytes;
+    mbar_arrive_expect_tx(&my_bars[s], kStageBytes);
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h)
+      tma_load_3d(st + h * kHalfBytes, &kmap, kvh * D + h * 64, off, blk, &my_bars[s]);
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h)
+      tma_load_3d(st + (kHalves + h) * kHalfBytes, &vmap, kvh * D + h * 64, off, blk, &my_bars[s]);
+  };
+  if (lane == 0) {
+    const int pre = my_tiles < kStages ? my_tiles : kStages;
+    for (int k = 0; k < pre; ++k) issue(k);
+  }
+
+  int k = 0;        // tiles consumed
+  int k_fail = -1;  // first tile whose wait gave up
+  int b = b_first;
+  int64_t ob = o_first;
+  while (ob < r1) {
+    const int64_t len = len_of(b);
+    const int64_t nt = (len + kTile - 1) / kTile;
+    if (nt == 0) {  // an empty sequence has no tile in any range (the merge kernel writes its zeros)
+      ++b;
+      continue;
+    }
+    const int64_t g0 = max(ob, r0), g1 = min(ob + nt, r1);
+    const int32_t* table = a.block_table + (int64_t)b * a.bt_stride;
+    // fused write: the range holding the sequence's last tile writes this step's K/V row
+    int64_t new_row = -1;
+    if (a.k_new != nullptr && g1 == ob + nt) {
+      const int64_t last = len - 1;
+      const int64_t s_new = __ldg(a.slot_mapping + b);
+      const int blk_last = __ldg(table + (last >> a.block_shift));
+      const int64_t expect = (blk_last >= 0 && blk_last < a.num_blocks)
+                                 ? ((int64_t)blk_last << a.block_shift) + (last & bmask) : -2;
+      if (s_new >= 0) {
+        if (s_new == expect)
+          new_row = (int64_t)blk_last * a.kv_block_stride + (last & bmask) * ((int64_t)a.n_kv_heads * D);
+        else if (lane == 0)
+          raise_error(a.err, PA_DEVERR_SLOT);
+      }
+    }
+    uint32_t qa[kKSteps][2];
+    load_q_frags<T, D, G>(a, b, kvh, lane, qa);
+    float o[kDTiles][4];
+#pragma unroll
+    for (int i = 0; i < kDTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool have = false;
+    for (int64_t u = g0; u < g1; ++u, ++k) {
+      if (k_fail >= 0) continue;
+      const int s = k % kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&my_bars[s], (unsigned)((k / kStages) & 1), a.err))) {
+        k_fail = k;
+        continue;
+      }
+      const int64_t t0 = (u - ob) * kTile;
+      const int blk = __ldg(table + (t0 >> a.block_shift));
+      const int valid = (int)(len - t0 < kTile ? len - t0 : kTile);
+      uint8_t* st = my_stages + s * kStageBytes;
+      if (blk >= 0 && blk < a.num_blocks) {
+        if (new_row >= 0 && u == ob + nt - 1) {
+          const int64_t src_off = ((int64_t)b * a.n_kv_heads + kvh) * D;
+          const int64_t dst_off = new_row + (int64_t)kvh * D;
+          patch_new_token<T, D>(st, (int)((len - 1) & (kTile - 1)), static_cast<const T*>(a.k_new) + src_off,
+                                static_cast<const T*>(a.v_new) + src_off, static_cast<T*>(a.k_pool_w) + dst_off,
+                                static_cast<T*>(a.v_pool_w) + dst_off, lane);
+        }
+        tile_update<T, D>(st, valid, qa, o, m_run, l_run, a.scale_log2, lane);
+        have = true;
+      }
+      // release the stage and refill it with the range's tile k + kStages
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && k + kStages < my_tiles) issue(k + kStages);
+    }
+    // ---- segment end: output or partial state of rows g < G (query heads of this KV head) --------
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    const float l_out = have && k_fail < 0 ? l_run : 0.f;
+    const bool whole = g0 == ob && g1 == ob + nt;
+    const int64_t q_first = ob / per;
+    if (g < G) {
+      const int64_t qh = (int64_t)b * a.n_q_heads + (int64_t)kvh * G + g;
+      if (whole) {
+        const float inv = l_out != 0.f ? 1.f / l_out : 0.f;
+        T* orow = static_cast<T*>(a.out) + qh * D;
+#pragma unroll
+        for (int i = 0; i < kDTiles; ++i) {
+          T* dst = orow + i * 8 + 2 * tig;
+          dst[0] = Elt<T>::from_float(o[i][0] * inv);
+          dst[1] = Elt<T>::from_float(o[i][1] * inv);
+        }
+      } else {
+        const int64_t pi = qh * a.max_parts + (q_unit - q_first);
+        float* acc = a.ws_acc + pi * D;
+#pragma unroll
+        for (int i = 0; i < kDTiles; ++i)
+          *reinterpret_cast<float2*>(acc + i * 8 + 2 * tig) = make_float2(o[i][0], o[i][1]);
+        if (tig == 0) {
+          a.ws_m[pi] = m_run;
+          a.ws_l[pi] = l_out;
+        }
+      }
+    }
+    if (kvh == 0 && g0 == ob && lane == 0) a.ws_np[b] = whole ? 1 : (int)((ob + nt - 1) / per - q_first + 1);
+    ob += nt;
+    ++b;
+  }
+  if (k_fail >= 0 && lane == 0) {
+    raise_error(a.err, PA_DEVERR_TIMEOUT);
+    // leave no copy in flight: wait (bounded) for the tiles issued from k_fail on
+    for (int j = k_fail; j < issued; ++j) mbar_wait(&my_bars[j % kStages], (unsigned)((j / kStages) & 1));
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
 // host side: tensor maps and dispatch
 // ------------------------------------------------------------------------------------------------
 namespace {
@@ -482,9 +776,14 @@ static cudaError_t launch_tc_g(const AttnArgs& a, const CUtensorMap& km, const C
     attr[0].val.clusterDim.x = (unsigned)a.max_parts;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+  } else {
+    // programmatic dependent launch: the grid may start while the preceding kernel of the stream
+    // (typically the previous step's merge) finishes; the kernel waits for it before any global access
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
   }
+  cfg.attrs = attr;
+  cfg.numAttrs = kCluster || PA_DECODE_PDL ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, D, G, kCluster>, a, km, vm);
 }
 
@@ -516,6 +815,75 @@ cudaError_t launch_decode_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int
       !encode_pool_map(&vm, a.v_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride))
     return cudaErrorInvalidValue;
   cudaError_t e = dt == PA_BF16 ? launch_tc_t<__nv_bfloat16>(a, km, vm, s) : launch_tc_t<__half>(a, km, vm, s);
+  ++*launches;
+  return e;
+}
+
+template <typename T, int D, int G>
+static cudaError_t launch_bal_g(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
+  constexpr int smem = 1024 /*barriers*/ + 1024 /*alignment*/ + kTcWarps * TcCfg<D>::kStages * TcCfg<D>::kStageBytes;
+  static int ctas_per_sm[64] = {};  // per instantiation and device: resident CTAs per SM at this smem
+  static int sm_count[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int per_sm = dev >= 0 && dev < 64 ? ctas_per_sm[dev] : 0;
+  int sms = dev >= 0 && dev < 64 ? sm_count[dev] : 0;
+  if (per_sm == 0 || sms == 0) {
+    e = cudaFuncSetAttribute(decode_bal_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_bal_kernel<T, D, G>, kTcWarps * 32, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    if (dev >= 0 && dev < 64) {
+      ctas_per_sm[dev] = per_sm;
+      sm_count[dev] = sms;
+    }
+  }
+  // one wave: n_ctas ranges per KV head, n_ctas x n_kv_heads CTAs resident together
+  int64_t n_ctas = (int64_t)per_sm * sms / a.n_kv_heads;
+  if (n_ctas < 1) n_ctas = 1;
+  const int64_t grid = n_ctas * a.n_kv_heads;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kTcWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // as in launch_tc_g
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PA_DECODE_PDL ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, decode_bal_kernel<T, D, G>, a, km, vm);
+}
+
+template <typename T, int D>
+static cudaError_t launch_bal_d(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
+  switch (a.group) {
+    case 1: return launch_bal_g<T, D, 1>(a, km, vm, s);
+    case 2: return launch_bal_g<T, D, 2>(a, km, vm, s);
+    case 4: return launch_bal_g<T, D, 4>(a, km, vm, s);
+    case 8: return launch_bal_g<T, D, 8>(a, km, vm, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+static cudaError_t launch_bal_t(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
+  return a.head_dim == 64 ? launch_bal_d<T, 64>(a, km, vm, s) : launch_bal_d<T, 128>(a, km, vm, s);
+}
+
+cudaError_t launch_decode_bal(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches) {
+  if (a.rows == 0) return cudaSuccess;
+  if (a.ws_np == nullptr || a.ws_acc == nullptr || a.max_parts < 2) return cudaErrorInvalidValue;
+  CUtensorMap km, vm;
+  if (!encode_pool_map(&km, a.k_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride) ||
+      !encode_pool_map(&vm, a.v_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride))
+    return cudaErrorInvalidValue;
+  cudaError_t e = dt == PA_BF16 ? launch_bal_t<__nv_bfloat16>(a, km, vm, s) : launch_bal_t<__half>(a, km, vm, s);
   ++*launches;
   return e;
 }

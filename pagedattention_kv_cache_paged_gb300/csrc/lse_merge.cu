@@ -22,13 +22,26 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
   constexpr int kPer = D / 32;
   const int64_t row = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  pdl_wait_primary();  // partials of the partition kernel are complete and visible
+  pdl_launch_dependents();  // the next step's decode grid may begin launching (it waits for this grid)
+  pdl_wait_primary();       // partials of the partition kernel are complete and visible
   if (row >= a.rows) return;
   int parts = a.n_parts;
   if (a.context_lens != nullptr) {
     int64_t len = __ldg(a.context_lens + row / a.heads_per_seq);
     len = len < 0 ? 0 : (len > a.max_len ? a.max_len : len);
-    parts = len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
+    if (a.seq_parts != nullptr) {
+      // equal-work grid: an empty sequence met no range; the others say how many slots they use
+      if (len == 0) {
+        T* o = static_cast<T*>(a.out) + row * D + lane * kPer;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) o[i] = Elt<T>::from_float(0.f);
+        return;
+      }
+      parts = __ldg(a.seq_parts + row / a.heads_per_seq);
+      parts = parts > a.n_parts ? a.n_parts : parts;
+    } else {
+      parts = len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
+    }
     if (parts <= 1) return;  // written directly by the partition kernel
   }
   const float* pm = a.part_m + row * a.n_parts;

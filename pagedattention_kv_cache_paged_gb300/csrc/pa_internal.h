@@ -81,6 +81,9 @@ struct AttnArgs {
   float* ws_m;                     // [rows * n_q_heads][max_parts]
   float* ws_l;                     // [rows * n_q_heads][max_parts]
   float* ws_acc;                   // [rows * n_q_heads][max_parts][head_dim]
+  // equal-work decode grid only (nullptr otherwise): per sequence, the number of split-K slots its
+  // partial states occupy (1 = written directly); max_parts is then the slot stride per row
+  int32_t* ws_np;
   unsigned* err;
   // fused K/V write (decode only; all nullptr otherwise): sequence b's new token k_new[b], v_new[b]
   // ([batch][n_kv_heads][head_dim]) goes to pool row slot_mapping[b], which must be the slot of its
@@ -110,6 +113,9 @@ struct MergeArgs {
   int heads_per_seq;
   int part_tokens;
   int64_t max_len;                 // clamp for context_lens (bt_stride * block_size)
+  // equal-work decode grid: when seq_parts != nullptr (with context_lens), sequence s's rows hold
+  // seq_parts[s] partials (<= n_parts; 1 = written directly) and empty sequences are written as zeros
+  const int32_t* seq_parts;
 };
 
 // Launchers: return cudaSuccess or the launch error.  `launches` is incremented per kernel.
@@ -132,6 +138,9 @@ bool encode_q_map(CUtensorMap* map, const void* q, pa_dtype dt, int64_t total_q,
 // Tensor-core decode (TMA + mma.sync) for bf16/fp16 pools with block_size % 16 == 0.
 bool decode_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks);
 cudaError_t launch_decode_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
+// Equal-work split-K grid of the same kernel math (needs a.ws_np and the workspace; a.max_parts is
+// the slot stride per row, at least 2).
+cudaError_t launch_decode_bal(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
 
 // Tensor-core causal prefill (TMA ring + mma.sync) for bf16/fp16 pools with block_size % 16 == 0.
 bool prefill_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks);

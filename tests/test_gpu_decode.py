@@ -37,6 +37,7 @@ def _reset_options(cuda_lib):
     pa.set_option(pa.PA_OPT_DECODE_KERNEL, 0)
     pa.set_option(pa.PA_OPT_CHECKED, 0)
     pa.set_option(pa.PA_OPT_CLUSTER_MERGE, 0)
+    pa.set_option(pa.PA_OPT_DECODE_GRID, 0)
     pa.device_error_flags(clear=True)
 
 
@@ -186,6 +187,69 @@ def test_decode_shapes_and_partitions(cuda_lib, dtype, D, G, S, part, kernel):
     ref = oracle.paged_decode(case.q, kp1, vp1, case.block_table, case.context_lens, case.scale)
     assert_close(out, ref, dtype, f"{dtype} D{D} G{G} S{S} part{part} kernel{kernel}")
     assert pa.device_error_flags() == 0
+
+
+# history lengths of a ragged batch: empty, single-token, block-aligned and long sequences next to
+# each other, so that equal-work ranges start and end inside sequences, hold several short ones,
+# and long sequences meet many ranges
+RAGGED_HIST = [0, 3000, 0, 15, 16, 1, 2047, 0, 5, 700, 4000, 31, 32, 33, 1500, 0, 2, 1023, 1024, 1025]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("part", [0, 16, 64, 512])
+def test_decode_grids_on_a_ragged_batch_with_empty_sequences(cuda_lib, dtype, grid, part):
+    """Both split-K grids of the tensor-core decode (0: one CTA per partition, 1: equal work per
+    warp) against the oracle.  Sequences with history 0 are given context 0 (zeros out); part
+    16 gives 16-token partitions (and equal-work ranges of a few tiles), so long sequences spread
+    over hundreds of split-K slots."""
+    pa = cuda_lib
+    pa.set_option(pa.PA_OPT_DECODE_GRID, grid)
+    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, part)
+    case = _ragged_case(dtype, 32, 8, 128, 16, RAGGED_HIST, seed=21 + part)
+    lens = (case.context_lens - 1).clamp(min=0)  # history only: the new tokens are not written here
+    out = run_decode(pa, case, lens=lens)
+    ref = oracle.paged_decode(case.q, case.k_pool, case.v_pool, case.block_table, lens, case.scale)
+    assert_close(out, ref, dtype, f"grid {grid} part {part}")
+    empty = (lens == 0).nonzero().flatten()
+    assert torch.equal(out.cpu()[empty].float(), torch.zeros_like(out.cpu()[empty].float()))
+    assert pa.device_error_flags() == 0
+
+
+@pytest.mark.parametrize("G,D", [(1, 64), (2, 128), (4, 128), (8, 128), (8, 64)])
+def test_equal_work_grid_other_groups_and_head_dims(cuda_lib, G, D):
+    """The equal-work grid for every query-group size and head_dim."""
+    pa = cuda_lib
+    pa.set_option(pa.PA_OPT_DECODE_GRID, 1)
+    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 128)
+    Hkv = 4
+    case = _ragged_case(torch.bfloat16, Hkv * G, Hkv, D, 32, RAGGED_HIST, seed=40 + G * 3 + D)
+    dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
+    pa.paged_kv_write(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), dk, dv)
+    out = run_decode(pa, case, kp=dk, vp=dv)
+    kp1, vp1 = oracle.paged_kv_write(case.k_pool, case.v_pool, case.k_new, case.v_new, case.slot_mapping)
+    ref = oracle.paged_decode(case.q, kp1, vp1, case.block_table, case.context_lens, case.scale)
+    assert_close(out, ref, torch.bfloat16, f"G{G} D{D}")
+    assert pa.device_error_flags() == 0
+
+
+@pytest.mark.parametrize("grid", [0, 1])
+def test_split_decode_is_deterministic_and_stale_workspace_safe(cuda_lib, grid):
+    """Two calls on one workspace give the same bits, also after the workspace was filled with NaN
+    and after a call on a different batch (no state is carried from call to call)."""
+    pa = cuda_lib
+    pa.set_option(pa.PA_OPT_DECODE_GRID, grid)
+    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 64)
+    case = _ragged_case(torch.bfloat16, 32, 8, 128, 16, RAGGED_HIST, seed=23)
+    other = _ragged_case(torch.bfloat16, 32, 8, 128, 16, list(reversed(RAGGED_HIST)), seed=24)
+    nbytes = pa.decode_workspace_size(len(RAGGED_HIST), case.block_table.stride(0), 16, 32, 8, 128)
+    ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device="cuda").view(torch.uint8)
+    lens = (case.context_lens - 1).clamp(min=0)  # history only: the new tokens are not written here
+    out1 = run_decode(pa, case, lens=lens, workspace=ws).cpu()
+    run_decode(pa, other, lens=(other.context_lens - 1).clamp(min=0), workspace=ws)
+    out2 = run_decode(pa, case, lens=lens, workspace=ws).cpu()
+    assert torch.equal(bits(out1), bits(out2))
+    assert torch.isfinite(out1.float()).all()
 
 
 @pytest.mark.parametrize("dtype", DTYPES)

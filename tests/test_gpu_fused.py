@@ -25,6 +25,7 @@ def _reset(cuda_lib):
     cuda_lib.set_option(cuda_lib.PA_OPT_PARTITION_TOKENS, 0)
     cuda_lib.set_option(cuda_lib.PA_OPT_CHECKED, 0)
     cuda_lib.set_option(cuda_lib.PA_OPT_CLUSTER_MERGE, 0)
+    cuda_lib.set_option(cuda_lib.PA_OPT_DECODE_GRID, 0)
     cuda_lib.device_error_flags(clear=True)
 
 
@@ -51,11 +52,14 @@ def _both(pa, case, workspace="auto"):
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("D,G,S", [(128, 4, 16), (64, 1, 16), (128, 8, 32), (64, 2, 8)])
 @pytest.mark.parametrize("kernel", [0, 1])
-@pytest.mark.parametrize("split", [True, False, "cluster"])
+@pytest.mark.parametrize("split", [True, False, "cluster", "equal-work"])
 def test_fused_equals_write_then_decode(cuda_lib, dtype, D, G, S, kernel, split):
     pa = cuda_lib
     pa.set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
     pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 64)
+    if split == "equal-work":
+        pa.set_option(pa.PA_OPT_DECODE_GRID, 1)
+        split = True
     if split == "cluster":
         pa.set_option(pa.PA_OPT_CLUSTER_MERGE, 1)
         pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 128)
