@@ -36,10 +36,9 @@ HQ, HKV, D, S = 32, 8, 128, 16
 LLAMA_LAYERS = 32
 ELT = 2  # bf16
 # dram__bytes_read.sum + dram__bytes_write.sum of one paged_attention_decode_fused call on this
-# workload with separate pools and the per-partition grid (partition kernel 578.7 + 3.6 MB, merge
-# kernel 2.5 MB; mean of two calls), from one ncu capture of those three metrics.  Retake it whenever
-# either kernel changes.
-FUSED_CALL_DRAM_BYTES = 584.9e6
+# workload with separate pools and the per-partition grid, from one ncu capture of those metrics;
+# None until it is retaken for the current kernels (evict-first K/V loads, one-round-trip merge).
+FUSED_CALL_DRAM_BYTES = None
 
 
 def measured_peaks():

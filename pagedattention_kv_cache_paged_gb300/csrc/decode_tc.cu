@@ -53,6 +53,20 @@ namespace pa {
 #ifndef PA_DECODE_PDL
 #define PA_DECODE_PDL 1
 #endif
+// 1: K/V tiles are loaded with the L2 evict-first policy (read once), which keeps the split-K
+// partials L2-resident for the merge kernel
+#ifndef PA_KV_EVICT_FIRST
+#define PA_KV_EVICT_FIRST 1
+#endif
+
+// One TMA box of a K or V tile, with the evict-first policy when PA_KV_EVICT_FIRST is set.
+__device__ __forceinline__ void load_kv_box(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
+                                            uint64_t policy) {
+  if (PA_KV_EVICT_FIRST)
+    tma_load_3d_hint(dst, map, x, y, z, bar, policy);
+  else
+    tma_load_3d(dst, map, x, y, z, bar);
+}
 
 constexpr int kTcWarps = PA_TC_WARPS;
 constexpr int kTile = 16;          // tokens per tile (one mma k-step of PV)
@@ -272,6 +286,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   }
   __syncwarp();
 
+  const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once per launch
   auto issue = [&](int j) {  // lane 0 only
     const int s = j % kStages;
     const int blk = tile_block(j);
@@ -285,10 +300,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
     mbar_arrive_expect_tx(&my_bars[s], kStageBytes);
 #pragma unroll
     for (int h = 0; h < kHalves; ++h)
-      tma_load_3d(st + h * kHalfBytes, &kmap, kvh * D + h * 64, off, blk, &my_bars[s]);
+      load_kv_box(st + h * kHalfBytes, &kmap, kvh * D + h * 64, off, blk, &my_bars[s], kv_policy);
 #pragma unroll
     for (int h = 0; h < kHalves; ++h)
-      tma_load_3d(st + (kHalves + h) * kHalfBytes, &vmap, kvh * D + h * 64, off, blk, &my_bars[s]);
+      load_kv_box(st + (kHalves + h) * kHalfBytes, &vmap, kvh * D + h * 64, off, blk, &my_bars[s], kv_policy);
   };
   if (lane == 0) {
     const int pre = my_tiles < kStages ? my_tiles : kStages;
@@ -553,6 +568,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   int pb = b_first;
   int64_t pob = o_first, pnt = tiles_of(b_first);
   int issued = 0;
+  const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once per launch
   auto issue = [&](int k) {  // lane 0 only: the range's k-th tile
     const int64_t u = r0 + k;
     while (pob + pnt <= u) {
@@ -574,10 +590,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
     mbar_arrive_expect_tx(&my_bars[s], kStageBytes);
 #pragma unroll
     for (int h = 0; h < kHalves; ++h)
-      tma_load_3d(st + h * kHalfBytes, &kmap, kvh * D + h * 64, off, blk, &my_bars[s]);
+      load_kv_box(st + h * kHalfBytes, &kmap, kvh * D + h * 64, off, blk, &my_bars[s], kv_policy);
 #pragma unroll
     for (int h = 0; h < kHalves; ++h)
-      tma_load_3d(st + (kHalves + h) * kHalfBytes, &vmap, kvh * D + h * 64, off, blk, &my_bars[s]);
+      load_kv_box(st + (kHalves + h) * kHalfBytes, &vmap, kvh * D + h * 64, off, blk, &my_bars[s], kv_policy);
   };
   if (lane == 0) {
     const int pre = my_tiles < kStages ? my_tiles : kStages;

@@ -20,14 +20,31 @@ constexpr int kMergeWarps = 4;
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const MergeArgs a) {
   constexpr int kPer = D / 32;
+  constexpr int kSpec = 4;  // partitions whose accumulators are loaded before the count is known
   const int64_t row = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   pdl_launch_dependents();  // the next step's decode grid may begin launching (it waits for this grid)
   pdl_wait_primary();       // partials of the partition kernel are complete and visible
   if (row >= a.rows) return;
+  const float* pm = a.part_m + row * a.n_parts;
+  const float* pl = a.part_l + row * a.n_parts;
+  const float* pacc = a.part_acc + row * a.n_parts * (int64_t)D + lane * kPer;
+  // Every load that does not depend on the partition count goes out at once (one round trip to
+  // memory instead of three): the row's length and slot count, (max, sum) of partition `lane`, and
+  // this lane's head_dim slice of the first kSpec partitions' accumulators.
+  const int64_t seq = a.context_lens != nullptr ? row / a.heads_per_seq : 0;
+  int64_t len = a.context_lens != nullptr ? __ldg(a.context_lens + seq) : 0;
+  const int sp = a.seq_parts != nullptr ? __ldg(a.seq_parts + seq) : 0;
+  const float m_l = lane < a.n_parts ? pm[lane] : -INFINITY;
+  const float l_l = lane < a.n_parts ? pl[lane] : 0.f;
+  float accs[kSpec][kPer];
+#pragma unroll
+  for (int j = 0; j < kSpec; ++j)
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) accs[j][i] = j < a.n_parts ? pacc[(int64_t)j * D + i] : 0.f;
+
   int parts = a.n_parts;
   if (a.context_lens != nullptr) {
-    int64_t len = __ldg(a.context_lens + row / a.heads_per_seq);
     len = len < 0 ? 0 : (len > a.max_len ? a.max_len : len);
     if (a.seq_parts != nullptr) {
       // equal-work grid: an empty sequence met no range; the others say how many slots they use
@@ -37,19 +54,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
         for (int i = 0; i < kPer; ++i) o[i] = Elt<T>::from_float(0.f);
         return;
       }
-      parts = __ldg(a.seq_parts + row / a.heads_per_seq);
-      parts = parts > a.n_parts ? a.n_parts : parts;
+      parts = sp > a.n_parts ? a.n_parts : sp;
     } else {
       parts = len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
     }
     if (parts <= 1) return;  // written directly by the partition kernel
   }
-  const float* pm = a.part_m + row * a.n_parts;
-  const float* pl = a.part_l + row * a.n_parts;
-  const float* pacc = a.part_acc + row * a.n_parts * (int64_t)D + lane * kPer;
   // the row maximum over partitions that hold tokens: lane p looks at partitions p, p + 32, ...
-  float M = -INFINITY;
-  for (int p = lane; p < parts; p += 32)
+  float M = lane < parts && l_l != 0.f ? m_l : -INFINITY;
+  for (int p = lane + 32; p < parts; p += 32)
     if (pl[p] != 0.f) M = fmaxf(M, pm[p]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -63,15 +76,25 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
       const int p = p0 + lane;
       float w = 0.f;
       if (p < parts) {
-        const float lp = pl[p];
+        const float lp = p0 == 0 ? l_l : pl[p];
         if (lp != 0.f) {
-          w = fast_exp2(pm[p] - M);
+          w = fast_exp2((p0 == 0 ? m_l : pm[p]) - M);
           L = fmaf(lp, w, L);
         }
       }
       const int n = parts - p0 < 32 ? parts - p0 : 32;
+      if (p0 == 0) {
+#pragma unroll
+        for (int j = 0; j < kSpec; ++j) {
+          const float wj = __shfl_sync(0xffffffffu, w, j);
+          if (j < n && wj != 0.f) {
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) acc[i] = fmaf(accs[j][i], wj, acc[i]);
+          }
+        }
+      }
 #pragma unroll 4
-      for (int j = 0; j < n; ++j) {
+      for (int j = p0 == 0 ? kSpec : 0; j < n; ++j) {
         const float wj = __shfl_sync(0xffffffffu, w, j);
         if (wj != 0.f) {
           const float* src = pacc + (int64_t)(p0 + j) * D;
