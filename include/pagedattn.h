@@ -284,6 +284,21 @@ PA_API const char* pa_status_string(int status);
  * `stream`.  Returns the PA_DEVERR_* bits, or a negative status on a CUDA failure. */
 PA_API int pa_device_error_flags(int clear, void* stream);
 
+/*
+ * pa_selftest_bounded_wait — run the failure path of the library's bounded waits on the device.
+ * The pages have no counterpart: this is a test hook for the library itself.  Every pipelined kernel
+ * (TMA rings, tensor-memory hand-offs) waits on mbarriers with a time limit and, when one runs out,
+ * records PA_DEVERR_TIMEOUT and returns instead of hanging; the other waiting warps and CTAs see
+ * that bit and leave too.  This call launches one CTA that does exactly that on barriers nothing
+ * completes: warp 0 gives up after limit_ns and sets the bit, warp 1 (limit 1 s) must leave as soon
+ * as it sees it.  Nothing faults and the context stays usable.
+ *   limit_ns     warp 0's limit, 1000 .. 1000000000 (else PA_EINVAL)
+ *   elapsed_ns   optional device uint64_t[2]: how long warp 0's and warp 1's waits took
+ * Read the outcome with pa_device_error_flags(1, stream), which also clears the bit: while
+ * PA_DEVERR_TIMEOUT stays set, later waits that need more than a few tries give up early.
+ */
+PA_API int pa_selftest_bounded_wait(int64_t limit_ns, void* elapsed_ns, void* stream);
+
 /* Number of kernels this library has launched in this process (all devices). */
 PA_API uint64_t pa_launch_count(void);
 

@@ -49,6 +49,7 @@ SIGNATURES = {
     "pa_last_cuda_error": (_i32, []),
     "pa_status_string": (ctypes.c_char_p, [_i32]),
     "pa_device_error_flags": (_i32, [_i32, _vp]),
+    "pa_selftest_bounded_wait": (_i32, [_i64, _vp, _vp]),
     "pa_launch_count": (ctypes.c_uint64, []),
     "pa_version": (ctypes.c_char_p, []),
 }
@@ -388,6 +389,18 @@ def device_error_flags(clear: bool = True, stream=None) -> int:
     if v < 0:
         _check("pa_device_error_flags", v)
     return v
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None) -> tuple:
+    """Run the bounded-wait self-test (see pa_selftest_bounded_wait) and return (error flags,
+    warp 0's wait in ns, warp 1's wait in ns); the flags are read and cleared."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    elapsed = torch.zeros(2, dtype=torch.int64, device=dev)
+    _check("pa_selftest_bounded_wait",
+           load_library().pa_selftest_bounded_wait(int(limit_ns), elapsed.data_ptr(), _stream(stream)))
+    flags = device_error_flags(clear=True, stream=stream)
+    e = elapsed.cpu()
+    return flags, int(e[0]), int(e[1])
 
 
 def launch_count() -> int:

@@ -226,6 +226,18 @@ int pa_device_error_flags(int clear, void* stream) {
   return (int)v;
 }
 
+int pa_selftest_bounded_wait(int64_t limit_ns, void* elapsed_ns, void* stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000) return PA_EINVAL;
+  if (elapsed_ns != nullptr && (reinterpret_cast<uintptr_t>(elapsed_ns) & 7u) != 0) return PA_EINVAL;
+  unsigned* err = nullptr;
+  int rc = device_info(&err, nullptr);
+  if (rc) return rc;
+  int launches = 0;
+  cudaError_t e = launch_selftest_wait(err, (uint64_t)limit_ns, static_cast<unsigned long long*>(elapsed_ns),
+                                       static_cast<cudaStream_t>(stream), &launches);
+  return finish(e, launches);
+}
+
 int paged_kv_write(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens,
                    void* k_pool, void* v_pool, int64_t num_blocks, int block_size, int n_kv_heads,
                    int head_dim, pa_dtype dtype, void* stream) {

@@ -149,4 +149,8 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, in
 // tcgen05 causal prefill (TMEM accumulators, TMA ring, warp-specialised), same support set.
 cudaError_t launch_prefill_umma(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
 
+// Bounded-wait self-test (selftest.cu): one CTA whose two waits run out; see pa_selftest_bounded_wait.
+cudaError_t launch_selftest_wait(unsigned* err, uint64_t limit_ns, unsigned long long* elapsed_ns, cudaStream_t s,
+                                 int* launches);
+
 }  // namespace pa

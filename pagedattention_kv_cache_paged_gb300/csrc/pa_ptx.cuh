@@ -79,7 +79,8 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Bounded wait for the phase with the given parity to complete.  Between tries the wait also
 // watches `abort_word` (the device error word): once any CTA has recorded a timeout, the others stop
 // waiting too, so a broken launch ends after about one timeout period instead of one per CTA.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, const unsigned* abort_word = nullptr) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, unsigned parity, const unsigned* abort_word,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (unsigned n = 1;; ++n) {
@@ -89,9 +90,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, const 
       if (abort_word != nullptr &&
           (*reinterpret_cast<const volatile unsigned*>(abort_word) & 32u /* PA_DEVERR_TIMEOUT */))
         return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, const unsigned* abort_word = nullptr) {
+  return mbar_wait_for(bar, parity, abort_word, kWaitLimitNs);
 }
 
 // 2-D tiled TMA load global -> shared, completing `bytes` on `bar`.  x is the inner coordinate.
