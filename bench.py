@@ -33,6 +33,7 @@ import workloads as W  # noqa: E402
 METRIC = "paged decode attn: KV GB/s (% HBM roofline) and decode tok/s, Llama-3-8B GQA"
 UNIT = "GB/s"
 HQ, HKV, D, S = 32, 8, 128, 16
+SEED_LONG = 1004  # seed of the long-context configuration's device inputs
 LLAMA_LAYERS = 32
 ELT = 2  # bf16
 # dram__bytes_read.sum + dram__bytes_write.sum of one paged_attention_decode_fused call on this
@@ -312,6 +313,142 @@ def run_prefill(args):
     return 0
 
 
+def _timed_fused_decode(pa, lib, *, lens, Hq, Hkv, Dh, S, dtype, code, pools_count, num_blocks, max_blocks, reps,
+                        warmup, seed, flush_bytes):
+    """Median device time of one paged_attention_decode_fused call (CUDA events around the call on
+    its stream), over ``reps`` calls that rotate through ``pools_count`` independent pools, with an
+    L2 flush (a write of ``flush_bytes``) between calls when that is non-zero."""
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    inp = W.device_decode_inputs(lens, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=Dh, block_size=S, dtype=dtype,
+                                 num_blocks=num_blocks, max_blocks_per_seq=max_blocks, device=dev, seed=seed,
+                                 layers=pools_count)
+    table, ctx, slot = inp["block_table"].to(dev), inp["context_lens"].to(dev), inp["slot_mapping"].to(dev)
+    q, kn, vn = inp["q"].to(dev), inp["k_new"].to(dev), inp["v_new"].to(dev)
+    out = torch.empty_like(q)
+    B = len(lens)
+    ws_bytes = pa.decode_workspace_size(B, table.stride(0), S, Hq, Hkv, Dh)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(max(flush_bytes // 4, 1), dtype=torch.float32, device=dev) if flush_bytes else None
+    scale = 1.0 / math.sqrt(Dh)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def call(i):
+        kp, vp = inp["pools"][i % pools_count]
+        st = lib.paged_attention_decode_fused(out.data_ptr(), q.data_ptr(), kn.data_ptr(), vn.data_ptr(),
+                                              slot.data_ptr(), kp.data_ptr(), vp.data_ptr(), table.data_ptr(),
+                                              table.stride(0), ctx.data_ptr(), B, num_blocks, S, scale, Hq, Hkv, Dh,
+                                              code, ws.data_ptr(), ws_bytes, sp)
+        if st:
+            raise RuntimeError(f"paged_attention_decode_fused status {st}")
+
+    times = []
+    for i in range(warmup + reps):
+        if flush is not None:
+            flush.fill_(float(i))
+        e0.record(stream)
+        call(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= warmup:
+            times.append(e0.elapsed_time(e1))
+    del inp
+    return statistics.median(times)
+
+
+def run_long(args):
+    """Long-context split-K decode: batch 4 at 32K/64K/96K/128K tokens, 32 query / 8 KV heads,
+    head_dim 128, block_size 16, bf16; one step = one fused write + decode call (the split-K
+    partition kernel and the log-sum-exp merge).  Inputs are larger than L2 (1.34 GB of K/V per
+    call, two rotating pools)."""
+    import pagedattention_kv_cache_paged_gb300 as pa
+    lib = pa.load_library()
+    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, args.partition_tokens)
+    lens = list(W.LONG_LENS)
+    need = sum(W.ceil_div(n, S) for n in lens)
+    nb = W.ceil_div(5 * need, 4)
+    clocks = ClockSampler(0)
+    launches0 = pa.launch_count()
+    clocks.start()
+    ms = _timed_fused_decode(pa, lib, lens=lens, Hq=HQ, Hkv=HKV, Dh=D, S=S, dtype=torch.bfloat16, code=pa.PA_BF16,
+                             pools_count=2, num_blocks=nb, max_blocks=W.ceil_div(max(lens), S), reps=args.steps,
+                             warmup=args.warmup, seed=SEED_LONG, flush_bytes=0)
+    clk = clocks.stop()
+    launches = pa.launch_count() - launches0
+    kvb, wb = algorithmic_bytes(lens, len(lens))
+    gbs = (kvb + wb) / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    if pa.device_error_flags() != 0:
+        raise RuntimeError("device error word set during the benchmark")
+    line = {
+        "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V, bf16)",
+        "config": {"workload": "long_context_split_k_decode: batch 4 at 32768/65536/98304/131072 tokens, 32q/8kv "
+                               "heads, head_dim 128, block_size 16, write + decode in one fused call",
+                   "context_tokens": sum(lens), "l2": "inputs larger than L2: 1.34 GB of K/V per call, 2 pools",
+                   "partition_tokens": args.partition_tokens or "auto (1024 at this shape)", "timing": "median of per-call CUDA events"},
+        "pct_hbm_measured": gbs / peak,
+        "decode_tok_s_attention_only": len(lens) / (LLAMA_LAYERS * ms * 1e-3),
+        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode_fused (partition + merge kernels)",
+                     "achieved": gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": None},
+        "gpu_launches": launches, "clocks": clk,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_gpt2(args):
+    """GPT-2-small-shaped decode sweep: 12 query = 12 KV heads, head_dim 64, block_size 16, fp16;
+    batch {1, 2, 4, 8} x context {128 .. 2048}; per cell the median device time of one layer's fused
+    write + decode call over 12 layer pools, with an L2 flush between calls (most cells fit in L2
+    and are launch-bound: their time is reported in us)."""
+    import pagedattention_kv_cache_paged_gb300 as pa
+    lib = pa.load_library()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    cells = []
+    peak, peak_kind = measured_peaks()
+    clocks = ClockSampler(0)
+    launches0 = pa.launch_count()
+    clocks.start()
+    for bi, batch in enumerate(W.GPT2_BATCHES):
+        for ci, context in enumerate(W.GPT2_CONTEXTS):
+            lens = [context] * batch
+            need = batch * W.ceil_div(context, 16)
+            ms = _timed_fused_decode(pa, lib, lens=lens, Hq=12, Hkv=12, Dh=64, S=16, dtype=torch.float16,
+                                     code=pa.PA_FP16, pools_count=W.GPT2_LAYERS, num_blocks=W.ceil_div(5 * need, 4),
+                                     max_blocks=W.ceil_div(context, 16), reps=args.steps, warmup=args.warmup,
+                                     seed=W.SEED_BASE + 2 + 31 * bi + ci, flush_bytes=2 * l2)
+            kv = batch * context * 12 * 64 * 2 * 2
+            qo = 2 * batch * 12 * 64 * 2
+            wb = batch * 12 * 64 * 2 * 2 * 2
+            gbs = (kv + qo + wb) / (ms * 1e-3) / 1e9
+            cells.append({"batch": batch, "context": context, "us_per_layer_call": ms * 1e3, "GB/s": gbs,
+                          "tok_s_attention_only_12_layers": batch / (W.GPT2_LAYERS * ms * 1e-3)})
+    clk = clocks.stop()
+    launches = pa.launch_count() - launches0
+    if pa.device_error_flags() != 0:
+        raise RuntimeError("device error word set during the benchmark")
+    big = cells[-1]
+    line = {
+        "metric": METRIC, "value": big["GB/s"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": big["us_per_layer_call"] / 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp16", "data": "synthetic (seeded N(0,1) Q/K/V, fp16)",
+        "config": {"workload": "gpt2_small_decode_sweep: 12q = 12kv heads, head_dim 64, block_size 16, fp16, "
+                               "batch {1,2,4,8} x context {128..2048}, 12 layer pools; value = batch 8 x 2048",
+                   "l2": "L2 flushed (write of 2x L2) before every timed call", "timing": "median of per-call CUDA events"},
+        "cells": cells,
+        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode_fused at batch 8 x 2048 (50 MB per call)",
+                     "achieved": big["GB/s"], "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": big["GB/s"] / peak, "traffic": None},
+        "gpu_launches": launches, "clocks": clk,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def run_swap(args):
     """Block swap between the device pool and a pinned host pool (the offload tier): 8192 blocks of the
     serving shape (32 KB of K and 32 KB of V each, 512 MB per direction) swapped out, then swapped
@@ -390,7 +527,7 @@ def main():
     ap.add_argument("--decode-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--decode-grid", type=int, default=0,
                     help="split-K grid of the tensor-core decode: 0 one CTA per partition, 1 equal work per warp")
-    ap.add_argument("--workload", choices=["decode", "prefill", "swap"], default="decode")
+    ap.add_argument("--workload", choices=["decode", "prefill", "swap", "long", "gpt2"], default="decode")
     ap.add_argument("--unfused", action="store_true",
                     help="time paged_kv_write + paged_attention_decode as two calls instead of the fused call")
     ap.add_argument("--prefill-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05, 3 mma.sync")
@@ -403,6 +540,10 @@ def main():
         return run_prefill(args)
     if args.workload == "swap":
         return run_swap(args)
+    if args.workload == "long":
+        return run_long(args)
+    if args.workload == "gpt2":
+        return run_gpt2(args)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 
@@ -597,7 +738,7 @@ def main():
                    "l2": f"inputs larger than L2: {args.layers} rotating layer pools, "
                          f"{kvb / 1e6:.0f} MB of K/V read per step",
                    "parallelism": f"replicas x{world}",
-                   "partition_tokens": args.partition_tokens or 1024,
+                   "partition_tokens": args.partition_tokens or "auto (1024 at this shape)",
                    "decode_kernel": ["auto", "cuda-core", "tensor-core"][args.decode_kernel],
                    "decode_grid": ["one CTA per partition", "equal work per warp"][args.decode_grid],
                    "kv_layout": args.kv_layout},

@@ -92,7 +92,9 @@ enum {
 enum {
   PA_OPT_CHECKED = 1,          /* 0 (default) or 1: host-side validation before each launch */
   PA_OPT_DECODE_KERNEL = 2,    /* 0 auto (default), 1 CUDA-core kernel, 2 tensor-core kernel */
-  PA_OPT_PARTITION_TOKENS = 3, /* 0 auto (default: 1024) or split-K partition length in tokens, rounded up to block_size */
+  PA_OPT_PARTITION_TOKENS = 3, /* split-K partition length in tokens, rounded up to block_size; 0 (default)
+                                  = automatic: about one wave of decode CTAs (456) when every row is
+                                  as long as the table allows, clamped to [256, 1024] tokens */
   PA_OPT_PREFILL_KERNEL = 4,   /* 0 auto (default), 1 CUDA-core kernel, 2 tcgen05 tensor-core kernel,
                                   3 mma.sync tensor-core kernel */
   PA_OPT_CLUSTER_MERGE = 5,    /* 0 (default) or 1: on the tensor-core decode path, rows split into 2-8

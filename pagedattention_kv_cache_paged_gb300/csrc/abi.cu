@@ -118,11 +118,23 @@ int validate_tables(const int32_t* block_table, int64_t bt_stride, const int32_t
   return PA_OK;
 }
 
-// Split-K plan: partition length in tokens and partitions per row.
-void plan_split(int64_t bt_stride, int block_size, int* part_tokens, int* max_parts) {
+// Split-K plan: partition length in tokens and partitions per row.  The automatic length gives the
+// grid about one wave of the tensor-core decode (3 resident CTAs per SM on 152 SMs) when every row
+// is as long as the table allows, between 256 tokens (four 16-token tiles per warp: below that the
+// merge launch costs more than the shorter partitions save) and 1024 (measured best at the serving
+// shape, where rows are long and many: shorter partitions there lose to per-CTA start-up and merge
+// traffic).  Small batches of long rows get short partitions and so enough CTAs to keep loads in
+// flight; a batch that fills the GPU anyway is not split further.
+constexpr int64_t kSplitTargetCtas = 3 * 152;
+
+void plan_split(int batch, int n_kv_heads, int64_t bt_stride, int block_size, int* part_tokens, int* max_parts) {
   const int64_t max_len = bt_stride * block_size;
   int64_t p = g_options[PA_OPT_PARTITION_TOKENS].load();
-  if (p <= 0) p = 1024;  // measured best for the tensor-core decode at serving shapes
+  if (p <= 0) {
+    const int64_t rows = (int64_t)(batch > 0 ? batch : 1) * (n_kv_heads > 0 ? n_kv_heads : 1);
+    p = (rows * max_len + kSplitTargetCtas - 1) / kSplitTargetCtas;
+    p = p < 256 ? 256 : (p > 1024 ? 1024 : p);
+  }
   p = ((p + block_size - 1) / block_size) * block_size;
   if (p >= max_len) {
     *part_tokens = (int)(max_len > 0 ? max_len : block_size);
@@ -276,10 +288,9 @@ int paged_kv_write(const void* k_new, const void* v_new, const int64_t* slot_map
 
 size_t paged_attention_decode_workspace_size(int batch, int64_t block_table_stride, int block_size,
                                              int n_q_heads, int n_kv_heads, int head_dim) {
-  (void)n_kv_heads;
   if (batch <= 0 || block_table_stride <= 0 || block_size <= 0 || n_q_heads <= 0 || head_dim <= 0) return 0;
   int part = 0, max_parts = 1;
-  plan_split(block_table_stride, block_size, &part, &max_parts);
+  plan_split(batch, n_kv_heads, block_table_stride, block_size, &part, &max_parts);
   return workspace_layout(batch, (int64_t)batch * n_q_heads, max_parts, head_dim).bytes;
 }
 
@@ -335,7 +346,7 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
   const bool use_tc = kernel_opt == 2 || (kernel_opt == 0 && tc_ok);
 
   int part_tokens = 0, max_parts = 1;
-  plan_split(block_table_stride, block_size, &part_tokens, &max_parts);
+  plan_split(batch, n_kv_heads, block_table_stride, block_size, &part_tokens, &max_parts);
   WsLayout ws = workspace_layout(batch, (int64_t)batch * n_q_heads, max_parts, head_dim);
   // up to 8 partitions per row on the tensor-core path: one thread-block cluster per row merges
   // through distributed shared memory, with neither workspace nor merge kernel
