@@ -365,6 +365,7 @@ def run_long(args):
     import pagedattention_kv_cache_paged_gb300 as pa
     lib = pa.load_library()
     pa.set_option(pa.PA_OPT_PARTITION_TOKENS, args.partition_tokens)
+    pa.set_option(pa.PA_OPT_DECODE_GRID, args.decode_grid)
     lens = list(W.LONG_LENS)
     need = sum(W.ceil_div(n, S) for n in lens)
     nb = W.ceil_div(5 * need, 4)
@@ -388,7 +389,9 @@ def run_long(args):
         "config": {"workload": "long_context_split_k_decode: batch 4 at 32768/65536/98304/131072 tokens, 32q/8kv "
                                "heads, head_dim 128, block_size 16, write + decode in one fused call",
                    "context_tokens": sum(lens), "l2": "inputs larger than L2: 1.34 GB of K/V per call, 2 pools",
-                   "partition_tokens": args.partition_tokens or "auto (1024 at this shape)", "timing": "median of per-call CUDA events"},
+                   "partition_tokens": args.partition_tokens or "auto (1024 at this shape)",
+                   "decode_grid": ["one CTA per partition", "equal work per warp"][args.decode_grid],
+                   "timing": "median of per-call CUDA events"},
         "pct_hbm_measured": gbs / peak,
         "decode_tok_s_attention_only": len(lens) / (LLAMA_LAYERS * ms * 1e-3),
         "roofline": {"bound": "hbm", "kernel": "paged_attention_decode_fused (partition + merge kernels)",
