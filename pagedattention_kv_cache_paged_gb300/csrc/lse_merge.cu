@@ -9,7 +9,10 @@
 // token and are skipped; a row with none left is written as zeros.  A NaN anywhere in a partition
 // propagates to the output, as it does in the two-pass definition.
 //
-// One warp per output row; lanes own head_dim / 32 consecutive elements.
+// Few partitions per row (n_parts < kWideParts): one warp per output row; lanes own head_dim / 32
+// consecutive elements.  Many (long contexts): one CTA of kWideWarps warps per row, the warps
+// taking every kWideWarps-th partition with several 16-byte loads in flight each, then summing
+// their shares in shared memory; the result is the same identity, summed in another order.
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -112,6 +115,98 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
   for (int i = 0; i < kPer; ++i) o[i] = Elt<T>::from_float(acc[i] * inv);
 }
 
+constexpr int kWideParts = 16;
+constexpr int kWideWarps = 8;
+
+// Number of partitions of row `row` that hold partial states (0: the row is empty and was written
+// here as zeros; 1: written directly by the partition kernel); shared by both merge kernels.
+template <typename T, int D>
+__device__ __forceinline__ int merge_parts(const MergeArgs& a, int64_t row, int tid, int nthreads) {
+  if (a.context_lens == nullptr) return a.n_parts;
+  const int64_t seq = row / a.heads_per_seq;
+  int64_t len = __ldg(a.context_lens + seq);
+  len = len < 0 ? 0 : (len > a.max_len ? a.max_len : len);
+  if (a.seq_parts != nullptr) {
+    if (len == 0) {
+      T* o = static_cast<T*>(a.out) + row * D;
+      for (int i = tid; i < D; i += nthreads) o[i] = Elt<T>::from_float(0.f);
+      return 0;
+    }
+    const int sp = __ldg(a.seq_parts + seq);
+    return sp > a.n_parts ? a.n_parts : sp;
+  }
+  return len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kWideWarps * 32) lse_merge_wide_kernel(const MergeArgs a) {
+  constexpr int kPer = D / 32;  // elements per lane: 4 (one 16-byte load) or 2 (8 bytes)
+  __shared__ float s_red[kWideWarps];
+  __shared__ float s_acc[kWideWarps][D];
+  __shared__ float s_l[kWideWarps];
+  const int64_t row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();  // the next step's decode grid may begin launching (it waits for this grid)
+  pdl_wait_primary();       // partials of the partition kernel are complete and visible
+  const int parts = merge_parts<T, D>(a, row, threadIdx.x, kWideWarps * 32);  // uniform over the CTA
+  if (parts <= 1) return;
+  const float* pm = a.part_m + row * a.n_parts;
+  const float* pl = a.part_l + row * a.n_parts;
+  const float* pacc = a.part_acc + row * a.n_parts * (int64_t)D + lane * kPer;
+  // the row maximum over partitions that hold tokens
+  float M = -INFINITY;
+  for (int p = threadIdx.x; p < parts; p += kWideWarps * 32)
+    if (pl[p] != 0.f) M = fmaxf(M, pm[p]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) s_red[warp] = M;
+  __syncthreads();
+  M = s_red[0];
+#pragma unroll
+  for (int w = 1; w < kWideWarps; ++w) M = fmaxf(M, s_red[w]);
+  // warp w: partitions w, w + kWideWarps, ...
+  float L = 0.f;
+  float acc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll 4
+    for (int p = warp; p < parts; p += kWideWarps) {
+      const float lp = pl[p];
+      if (lp != 0.f) {
+        const float wp = fast_exp2(pm[p] - M);
+        L = fmaf(lp, wp, L);
+        const float* src = pacc + (int64_t)p * D;
+        if constexpr (kPer == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          acc[0] = fmaf(v.x, wp, acc[0]);
+          acc[1] = fmaf(v.y, wp, acc[1]);
+          acc[2] = fmaf(v.z, wp, acc[2]);
+          acc[3] = fmaf(v.w, wp, acc[3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) acc[i] = fmaf(src[i], wp, acc[i]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) s_acc[warp][lane * kPer + i] = acc[i];
+  if (lane == 0) s_l[warp] = L;  // every lane of the warp holds the same L
+  __syncthreads();
+  float Lt = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWideWarps; ++w) Lt += s_l[w];
+  const float inv = Lt != 0.f ? 1.f / Lt : 0.f;
+  T* o = static_cast<T*>(a.out) + row * D;
+  for (int d = threadIdx.x; d < D; d += kWideWarps * 32) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWideWarps; ++w) v += s_acc[w][d];
+    o[d] = Elt<T>::from_float(v * inv);
+  }
+}
+
 template <typename T, int D>
 static cudaError_t launch_merge_d(const MergeArgs& a, cudaStream_t s, unsigned blocks, bool pdl) {
   cudaLaunchConfig_t cfg = {};
@@ -124,13 +219,19 @@ static cudaError_t launch_merge_d(const MergeArgs& a, cudaStream_t s, unsigned b
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
+  // (the wide kernel reads each lane's slice with one 16-byte load: needs a 16-byte aligned base)
+  if (a.n_parts >= kWideParts && (reinterpret_cast<uintptr_t>(a.part_acc) & 15u) == 0) {
+    cfg.gridDim = dim3((unsigned)a.rows);
+    cfg.blockDim = dim3(kWideWarps * 32);
+    return cudaLaunchKernelEx(&cfg, lse_merge_wide_kernel<T, D>, a);
+  }
   return cudaLaunchKernelEx(&cfg, lse_merge_kernel<T, D>, a);
 }
 
 template <typename T>
 static cudaError_t launch_merge_t(const MergeArgs& a, cudaStream_t s) {
   const int64_t blocks = (a.rows + kMergeWarps - 1) / kMergeWarps;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (blocks > 0x7fffffffLL || (a.n_parts >= kWideParts && a.rows > 0x7fffffffLL)) return cudaErrorInvalidConfiguration;
   const bool pdl = a.context_lens != nullptr;  // internal merge right after the partition kernel
   switch (a.head_dim) {
     case 64: return launch_merge_d<T, 64>(a, s, (unsigned)blocks, pdl);

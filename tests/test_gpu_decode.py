@@ -361,15 +361,21 @@ def test_workspace_too_small_is_rejected(cuda_lib):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_lse_merge_matches_oracle_merge(cuda_lib, dtype):
+@pytest.mark.parametrize("D,many", [(128, False), (128, True), (64, True)])
+def test_lse_merge_matches_oracle_merge(cuda_lib, dtype, D, many):
+    """The standalone merge against the oracle's; `many` gives 40 partitions (the one-CTA-per-row
+    merge for rows of 16 or more partitions), some of them empty."""
     pa = cuda_lib
-    rng = np.random.default_rng(11)
-    H, D, n = 6, 128, 300
+    rng = np.random.default_rng(11 + D + many)
+    H, n = 6, 300
     q = rng.standard_normal((H, D))
     k = rng.standard_normal((n, H, D))
     k[rng.choice(n, 4, replace=False)] *= 8
     v = rng.standard_normal((n, H, D))
-    cuts = [0, 0, 50, 51, 51, 200, 300]  # includes empty partitions
+    if many:
+        cuts = [0, 0] + sorted(int(c) for c in rng.choice(np.arange(1, n), 37, replace=False)) + [n, n]
+    else:
+        cuts = [0, 0, 50, 51, 51, 200, 300]  # includes empty partitions
     parts = oracle.partition_partials(q, k, v, 0.3, list(zip(cuts[:-1], cuts[1:])))
     P = len(parts)
     log2e = 1.0 / math.log(2.0)
@@ -380,7 +386,7 @@ def test_lse_merge_matches_oracle_merge(cuda_lib, dtype):
                                        torch.tensor(pl, dtype=torch.float32).cuda(),
                                        torch.tensor(pacc, dtype=torch.float32).cuda(), out_dtype=dtype)
     torch.cuda.synchronize()
-    assert P == 6
+    assert P == (40 if many else 6)
     assert_close(out, oracle.lse_merge(parts), dtype, "merge")
 
 
