@@ -75,6 +75,32 @@ def test_prefill_ragged_chunks(cuda_lib, dtype, D, G, S, kernel):
     assert pa.device_error_flags() == 0
 
 
+@pytest.mark.parametrize("G,D", [(4, 128), (8, 64)])
+def test_prefill_many_items_per_cta(cuda_lib, G, D):
+    """More (64-token query block, KV head) items than SMs, so every CTA of the tcgen05 kernel
+    walks several items in turn (Q reloaded, O handed over between items) across ragged chunks,
+    empty chunks and chunk boundaries inside an item; all outputs against the oracle."""
+    pa = cuda_lib
+    rng = np.random.default_rng(31 + G + D)
+    B = 48
+    hist = [int(x) for x in rng.integers(0, 400, B)]
+    chunks = [int(x) for x in rng.integers(0, 180, B)]
+    chunks[3] = 0
+    chunks[7] = 1
+    Hkv = 8
+    need = sum(W.ceil_div(h + c, 16) for h, c in zip(hist, chunks))
+    case = W.varlen_prefill(4242 + G, hist_lens=hist, chunk_lens=chunks, block_size=16, n_q_heads=Hkv * G,
+                            n_kv_heads=Hkv, head_dim=D, dtype=torch.bfloat16, num_blocks=need + 9)
+    assert sum(chunks) // (256 // G) * Hkv > 2 * 152  # several items per CTA
+    out, _, _ = run_case(pa, case, kernel=0)
+    kp, vp = oracle_pools(case)
+    res = oracle.paged_prefill(case.q, case.query_start_loc, kp, vp, case.block_table, case.context_lens, case.scale)
+    idx = sorted(res)
+    assert len(idx) == case.q.shape[0]
+    assert_close(out[idx], np.stack([res[i] for i in idx]), torch.bfloat16, f"G{G} D{D}")
+    assert pa.device_error_flags() == 0
+
+
 @pytest.mark.parametrize("kernel", [0, 3])
 def test_prefill_cow_arm_small_equals_unshared_copy(cuda_lib, kernel):
     """Copy-on-write fork of a shared partial block: the forked sequences attend exactly like
