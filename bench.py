@@ -41,6 +41,10 @@ ELT = 2  # bf16
 # kernel 4.3 MB with the cold L2 of the capture; mean of two calls), from one ncu capture of those
 # metrics.  Retake it whenever either kernel changes.
 FUSED_CALL_DRAM_BYTES = 585.8e6
+# dram__bytes_read.sum + dram__bytes_write.sum of one tcgen05 prefill launch on the chunked-prefill
+# workload (554.7 + 237.0 MB), from one `ncu --set full` capture of the persistent kernel.  Retake it
+# whenever the kernel changes.
+PREFILL_DRAM_BYTES = 791.7e6
 
 
 def measured_peaks():
@@ -306,7 +310,8 @@ def run_prefill(args):
         "kernel_us": {"prefill_median": pf * 1e3, "step_incl_write": total_ms / K * 1e3},
         "roofline": {"bound": "tensor", "kernel": "paged_attention_prefill", "achieved": flops / (pf * 1e-3) / 1e12,
                      "peak": peak, "peak_kind": "measured bf16 dense (burst)", "unit": "TFLOP/s",
-                     "frac": flops / (pf * 1e-3) / 1e12 / peak, "traffic": None},
+                     "frac": flops / (pf * 1e-3) / 1e12 / peak,
+                     "traffic": PREFILL_DRAM_BYTES if args.prefill_kernel in (0, 2) else None},
         "gpu_launches": launches, "clocks": clk,
     }
     print(json.dumps(line))
