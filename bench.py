@@ -319,10 +319,13 @@ def run_prefill(args):
 
 
 def _timed_fused_decode(pa, lib, *, lens, Hq, Hkv, Dh, S, dtype, code, pools_count, num_blocks, max_blocks, reps,
-                        warmup, seed, flush_bytes):
+                        warmup, seed, flush_bytes, graph=False):
     """Median device time of one paged_attention_decode_fused call (CUDA events around the call on
     its stream), over ``reps`` calls that rotate through ``pools_count`` independent pools, with an
-    L2 flush (a write of ``flush_bytes``) between calls when that is non-zero."""
+    L2 flush (a write of ``flush_bytes``) between calls when that is non-zero.  With ``graph``, also
+    the median time per call of a CUDA graph holding one call per pool (a captured layer loop),
+    replayed ``reps`` times with the flush before each replay: (single-call ms, per-call ms in the
+    graph)."""
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -358,8 +361,34 @@ def _timed_fused_decode(pa, lib, *, lens, Hq, Hkv, Dh, S, dtype, code, pools_cou
         torch.cuda.synchronize()
         if i >= warmup:
             times.append(e0.elapsed_time(e1))
-    del inp
-    return statistics.median(times)
+    if not graph:
+        del inp
+        return statistics.median(times)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for i in range(pools_count):
+            kp, vp = inp["pools"][i]
+            st = lib.paged_attention_decode_fused(out.data_ptr(), q.data_ptr(), kn.data_ptr(), vn.data_ptr(),
+                                                  slot.data_ptr(), kp.data_ptr(), vp.data_ptr(), table.data_ptr(),
+                                                  table.stride(0), ctx.data_ptr(), B, num_blocks, S, scale, Hq, Hkv,
+                                                  Dh, code, ws.data_ptr(), ws_bytes, side.cuda_stream)
+            if st:
+                raise RuntimeError(f"paged_attention_decode_fused status {st} under capture")
+    torch.cuda.synchronize()
+    gtimes = []
+    for i in range(warmup + reps):
+        if flush is not None:
+            flush.fill_(float(i))
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= warmup:
+            gtimes.append(e0.elapsed_time(e1) / pools_count)
+    del g, inp
+    return statistics.median(times), statistics.median(gtimes)
 
 
 def run_long(args):
@@ -425,16 +454,19 @@ def run_gpt2(args):
         for ci, context in enumerate(W.GPT2_CONTEXTS):
             lens = [context] * batch
             need = batch * W.ceil_div(context, 16)
-            ms = _timed_fused_decode(pa, lib, lens=lens, Hq=12, Hkv=12, Dh=64, S=16, dtype=torch.float16,
-                                     code=pa.PA_FP16, pools_count=W.GPT2_LAYERS, num_blocks=W.ceil_div(5 * need, 4),
-                                     max_blocks=W.ceil_div(context, 16), reps=args.steps, warmup=args.warmup,
-                                     seed=W.SEED_BASE + 2 + 31 * bi + ci, flush_bytes=2 * l2)
+            ms, gms = _timed_fused_decode(pa, lib, lens=lens, Hq=12, Hkv=12, Dh=64, S=16, dtype=torch.float16,
+                                          code=pa.PA_FP16, pools_count=W.GPT2_LAYERS,
+                                          num_blocks=W.ceil_div(5 * need, 4), max_blocks=W.ceil_div(context, 16),
+                                          reps=args.steps, warmup=args.warmup, seed=W.SEED_BASE + 2 + 31 * bi + ci,
+                                          flush_bytes=2 * l2, graph=True)
             kv = batch * context * 12 * 64 * 2 * 2
             qo = 2 * batch * 12 * 64 * 2
             wb = batch * 12 * 64 * 2 * 2 * 2
             gbs = (kv + qo + wb) / (ms * 1e-3) / 1e9
             cells.append({"batch": batch, "context": context, "us_per_layer_call": ms * 1e3, "GB/s": gbs,
-                          "tok_s_attention_only_12_layers": batch / (W.GPT2_LAYERS * ms * 1e-3)})
+                          "tok_s_attention_only_12_layers": batch / (W.GPT2_LAYERS * ms * 1e-3),
+                          "us_per_layer_in_12_layer_graph": gms * 1e3,
+                          "GB/s_in_graph": (kv + qo + wb) / (gms * 1e-3) / 1e9})
     clk = clocks.stop()
     launches = pa.launch_count() - launches0
     if pa.device_error_flags() != 0:
@@ -446,7 +478,8 @@ def run_gpt2(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "fp16", "data": "synthetic (seeded N(0,1) Q/K/V, fp16)",
         "config": {"workload": "gpt2_small_decode_sweep: 12q = 12kv heads, head_dim 64, block_size 16, fp16, "
                                "batch {1,2,4,8} x context {128..2048}, 12 layer pools; value = batch 8 x 2048",
-                   "l2": "L2 flushed (write of 2x L2) before every timed call", "timing": "median of per-call CUDA events"},
+                   "l2": "L2 flushed (write of 2x L2) before every timed call or graph replay",
+                   "timing": "median of per-call CUDA events; also a CUDA graph of the 12 layers' calls, replayed, per call"},
         "cells": cells,
         "roofline": {"bound": "hbm", "kernel": "paged_attention_decode_fused at batch 8 x 2048 (50 MB per call)",
                      "achieved": big["GB/s"], "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
