@@ -127,8 +127,14 @@ int validate_tables(const int32_t* block_table, int64_t bt_stride, const int32_t
 // flight; a batch that fills the GPU anyway is not split further.
 constexpr int64_t kSplitTargetCtas = 3 * 152;
 
+// Longest context a table row can describe; context lengths are int32, so longer rows are capped.
+int64_t table_capacity(int64_t bt_stride, int block_size) {
+  const int64_t cap = bt_stride * block_size;
+  return cap < (int64_t)INT32_MAX ? cap : (int64_t)INT32_MAX;
+}
+
 void plan_split(int batch, int n_kv_heads, int64_t bt_stride, int block_size, int* part_tokens, int* max_parts) {
-  const int64_t max_len = bt_stride * block_size;
+  const int64_t max_len = table_capacity(bt_stride, block_size);
   int64_t p = g_options[PA_OPT_PARTITION_TOKENS].load();
   if (p <= 0) {
     const int64_t rows = (int64_t)(batch > 0 ? batch : 1) * (n_kv_heads > 0 ? n_kv_heads : 1);
@@ -354,7 +360,7 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
   if (max_parts > 1 && !cluster) {
     if (workspace == nullptr) {
       max_parts = 1;
-      part_tokens = (int)(block_table_stride * block_size);
+      part_tokens = (int)table_capacity(block_table_stride, block_size);
     } else if (workspace_bytes < ws.bytes || !aligned16(workspace)) {
       return PA_EWORKSPACE;
     }
@@ -506,7 +512,7 @@ int paged_attention_prefill(void* out, const void* q, const int32_t* query_start
   a.n_kv_heads = n_kv_heads;
   a.group = n_q_heads / n_kv_heads;
   a.head_dim = head_dim;
-  a.part_tokens = (int)(block_table_stride * block_size);
+  a.part_tokens = (int)table_capacity(block_table_stride, block_size);
   a.max_parts = 1;
   a.err = err;
   int launches = 0;
