@@ -181,10 +181,12 @@ def decode_workspace_size(batch: int, block_table_stride: int, block_size: int, 
                                                          n_kv_heads, head_dim))
 
 
-def _workspace(device: torch.device, nbytes: int) -> torch.Tensor | None:
+def _workspace(device: torch.device, nbytes: int, stream) -> torch.Tensor | None:
+    """The binding's own split-K workspace, one per (device, stream): calls on one stream run in
+    order and may share it; calls on different streams may overlap and must not."""
     if nbytes == 0:
         return None
-    key = (device.index if device.index is not None else torch.cuda.current_device())
+    key = (device.index if device.index is not None else torch.cuda.current_device(), _stream(stream))
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
         buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -214,7 +216,7 @@ def paged_attention_decode(q, k_pool, v_pool, block_table, context_lens, scale=N
     if block_table.stride(1) != 1:
         raise ValueError("block_table rows must be contiguous")
     if workspace == "auto":
-        ws = _workspace(q.device, decode_workspace_size(B, bt_stride, S, Hq, Hkv, D))
+        ws = _workspace(q.device, decode_workspace_size(B, bt_stride, S, Hq, Hkv, D), stream)
     else:
         ws = workspace
     ws_ptr = _dev(ws, "workspace", torch.uint8) if ws is not None else None
@@ -250,7 +252,8 @@ def paged_attention_decode_fused(q, k_new, v_new, slot_mapping, k_pool, v_pool, 
     if out is None:
         out = torch.empty_like(q)
     bt_stride = int(block_table.stride(0))
-    ws = _workspace(q.device, decode_workspace_size(B, bt_stride, S, Hq, Hkv, D)) if workspace == "auto" else workspace
+    ws = (_workspace(q.device, decode_workspace_size(B, bt_stride, S, Hq, Hkv, D), stream) if workspace == "auto"
+          else workspace)
     st = lib.paged_attention_decode_fused(
         _dev(out, "out", dt), _dev(q, "q", dt), _dev(k_new, "k_new", dt), _dev(v_new, "v_new", dt),
         _dev(slot_mapping, "slot_mapping", torch.int64), _pool(k_pool, "k_pool", dt), _pool(v_pool, "v_pool", dt),
