@@ -231,52 +231,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   const int g = lane >> 2;   // mma row group: query head g of the group
   const int tig = lane & 3;  // thread in group
 
-  // launched with programmatic serialization: wait for the preceding grid (its outputs may be this
-  // call's inputs, and its reads of out / workspace must end before this grid writes them)
-  pdl_wait_primary();
-  const int64_t max_len = a.bt_stride << a.block_shift;
-  const int b = (int)row;
-  int64_t len = __ldg(a.context_lens + b);
-  if (len < 0 || len > max_len) {
-    if (threadIdx.x == 0) raise_error(a.err, PA_DEVERR_CONTEXT_LEN);
-    len = len < 0 ? 0 : max_len;
-  }
-  const int n_parts_row = len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
-  if (!kCluster && part >= n_parts_row) return;
-  const bool active = part < n_parts_row;  // a cluster's surplus CTAs stay for the barriers
-  const int64_t t_begin = (int64_t)part * a.part_tokens;
-  const int64_t t_end = active ? min(t_begin + a.part_tokens, len) : t_begin;
-  const int n_tiles = (int)((t_end - t_begin + kTile - 1) / kTile);
-  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kTcWarps - 1) / kTcWarps : 0;
-
-  const int32_t* table = a.block_table + (int64_t)b * a.bt_stride;
-  const int bmask = a.block_size - 1;
-  // fused write: the CTA holding the last context position writes this step's K/V row of its KV
-  // head there and uses it straight from k_new / v_new (nanoserve Day 19, "What I added today":
-  // write this step's K/V, then attend over the whole history)
-  int64_t new_row = -1;  // element offset of the new token's pool row
-  if (a.k_new != nullptr && len > 0 && part == n_parts_row - 1) {
-    const int64_t last = len - 1;
-    const int64_t s_new = __ldg(a.slot_mapping + b);
-    const int blk_last = __ldg(table + (last >> a.block_shift));
-    const int64_t expect = (blk_last >= 0 && blk_last < a.num_blocks)
-                               ? ((int64_t)blk_last << a.block_shift) + (last & bmask) : -2;
-    if (s_new >= 0) {
-      if (s_new == expect)
-        new_row = (int64_t)blk_last * a.kv_block_stride + (last & bmask) * ((int64_t)a.n_kv_heads * D);
-      else if (threadIdx.x == 0)
-        raise_error(a.err, PA_DEVERR_SLOT);
-    }
-  }
-  const int patch_tile = new_row >= 0 ? (int)((len - 1 - t_begin) / kTile) : -1;
+  // set-up that reads no global memory: this warp's ring barriers and the tensor maps
   uint64_t* my_bars = bars + warp * kStages;
   uint8_t* my_stages = stages + warp * kStages * kStageBytes;
-
-  // tile j of this warp covers tokens [tile_t0(j), tile_t0(j) + 16)
-  auto tile_t0 = [&](int j) -> int64_t { return t_begin + (int64_t)(warp + kTcWarps * j) * kTile; };
-  auto tile_block = [&](int j) -> int { return __ldg(table + (tile_t0(j) >> a.block_shift)); };
-
-  pdl_launch_dependents();  // the split-K merge may begin launching; it waits for this grid's results
   if (lane == 0) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
@@ -286,10 +243,43 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   }
   __syncwarp();
 
+  // launched with programmatic serialization: wait for the preceding grid (its outputs may be this
+  // call's inputs, and its reads of out / workspace must end before this grid writes them)
+  pdl_wait_primary();
+  const int64_t max_len = a.bt_stride << a.block_shift;
+  const int b = (int)row;
+  const int32_t* table = a.block_table + (int64_t)b * a.bt_stride;
+  const int64_t t_begin = (int64_t)part * a.part_tokens;
+  // tile j of this warp covers tokens [tile_t0(j), tile_t0(j) + 16)
+  auto tile_t0 = [&](int j) -> int64_t { return t_begin + (int64_t)(warp + kTcWarps * j) * kTile; };
+  auto tile_block = [&](int j) -> int { return __ldg(table + (tile_t0(j) >> a.block_shift)); };
+  // The loads that do not depend on one another go out together, so that their latencies overlap:
+  // the context length, the table entries of this warp's first tiles (read ahead of the length:
+  // every position below the table's capacity has an entry) and the Q fragments.
+  int64_t len = __ldg(a.context_lens + b);
+  int blk_first[kStages];
+#pragma unroll
+  for (int j = 0; j < kStages; ++j)
+    blk_first[j] = (lane == 0 && tile_t0(j) < max_len) ? tile_block(j) : -1;
+  uint32_t qa[kKSteps][2];
+  load_q_frags<T, D, G>(a, row, kvh, lane, qa);
+  if (len < 0 || len > max_len) {
+    if (threadIdx.x == 0) raise_error(a.err, PA_DEVERR_CONTEXT_LEN);
+    len = len < 0 ? 0 : max_len;
+  }
+  const int n_parts_row = len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
+  if (!kCluster && part >= n_parts_row) return;
+  const bool active = part < n_parts_row;  // a cluster's surplus CTAs stay for the barriers
+  const int64_t t_end = active ? min(t_begin + a.part_tokens, len) : t_begin;
+  const int n_tiles = (int)((t_end - t_begin + kTile - 1) / kTile);
+  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kTcWarps - 1) / kTcWarps : 0;
+  const int bmask = a.block_size - 1;
+
+  pdl_launch_dependents();  // the split-K merge may begin launching; it waits for this grid's results
+
   const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once per launch
-  auto issue = [&](int j) {  // lane 0 only
+  auto issue = [&](int j, int blk) {  // lane 0 only; blk = the table entry of tile j
     const int s = j % kStages;
-    const int blk = tile_block(j);
     if (blk < 0 || blk >= a.num_blocks) {
       raise_error(a.err, PA_DEVERR_BLOCK_ID);
       mbar_arrive(&my_bars[s]);  // complete the phase without data; the consumer skips the tile
@@ -307,11 +297,30 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   };
   if (lane == 0) {
     const int pre = my_tiles < kStages ? my_tiles : kStages;
-    for (int j = 0; j < pre; ++j) issue(j);
+#pragma unroll
+    for (int j = 0; j < kStages; ++j)
+      if (j < pre) issue(j, blk_first[j]);
   }
 
-  uint32_t qa[kKSteps][2];
-  load_q_frags<T, D, G>(a, row, kvh, lane, qa);
+  // fused write: the CTA holding the last context position writes this step's K/V row of its KV
+  // head there and uses it straight from k_new / v_new (nanoserve Day 19, "What I added today":
+  // write this step's K/V, then attend over the whole history).  Looked up once the first copies
+  // are on their way.
+  int64_t new_row = -1;  // element offset of the new token's pool row
+  if (a.k_new != nullptr && len > 0 && part == n_parts_row - 1) {
+    const int64_t last = len - 1;
+    const int64_t s_new = __ldg(a.slot_mapping + b);
+    const int blk_last = __ldg(table + (last >> a.block_shift));
+    const int64_t expect = (blk_last >= 0 && blk_last < a.num_blocks)
+                               ? ((int64_t)blk_last << a.block_shift) + (last & bmask) : -2;
+    if (s_new >= 0) {
+      if (s_new == expect)
+        new_row = (int64_t)blk_last * a.kv_block_stride + (last & bmask) * ((int64_t)a.n_kv_heads * D);
+      else if (threadIdx.x == 0)
+        raise_error(a.err, PA_DEVERR_SLOT);
+    }
+  }
+  const int patch_tile = new_row >= 0 ? (int)((len - 1 - t_begin) / kTile) : -1;
 
   float o[kDTiles][4];
 #pragma unroll
@@ -346,7 +355,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
     // release the stage and refill it with this warp's tile j + kStages
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0 && j + kStages < my_tiles) issue(j + kStages);
+    if (lane == 0 && j + kStages < my_tiles) issue(j + kStages, tile_block(j + kStages));
   }
   if (timed_out && lane == 0) {
     raise_error(a.err, PA_DEVERR_TIMEOUT);
