@@ -306,7 +306,9 @@ def run_prefill(args):
         "config": {"workload": "chunked prefill: 128 seqs, 1024-token shared prefix (32 blocks of 32, refcount "
                                "128), suffix U[0,512], causal chunk of 256, 32q/8kv heads, head_dim 128",
                    "prefill_kernel": ["auto (tcgen05)", "cuda-core", "tcgen05", "mma.sync"][args.prefill_kernel],
-                   "gflop_per_step": flops / 1e9, "steps_synchronised": True},
+                   "gflop_per_step": flops / 1e9, "steps_synchronised": True,
+                   "l2": "inputs larger than L2: per step 268 MB of queries, 134 MB of chunk K/V written, "
+                         "a 537 MB pool read"},
         "kernel_us": {"prefill_median": pf * 1e3, "step_incl_write": total_ms / K * 1e3},
         "roofline": {"bound": "tensor", "kernel": "paged_attention_prefill", "achieved": flops / (pf * 1e-3) / 1e12,
                      "peak": peak, "peak_kind": "measured bf16 dense (burst)", "unit": "TFLOP/s",
@@ -548,7 +550,8 @@ def run_swap(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "swap_blocks: 8192 blocks x (32 KB K + 32 KB V) device -> pinned host, then "
                                    "host -> device into other blocks (Llama-3-8B pool shape)",
-                       "bytes_per_direction": moved},
+                       "bytes_per_direction": moved,
+                       "l2": "inputs larger than L2: 537 MB moved each way per step"},
             "swap_out_gbs": moved * K / (t_out * 1e-3) / 1e9, "swap_in_gbs": moved * K / (t_in * 1e-3) / 1e9,
             "gpu_launches": launches, "clocks": clk}
     print(json.dumps(line))
