@@ -41,7 +41,7 @@
  * Dtypes.  q, pools and out share one dtype (PA_BF16, PA_FP16 or PA_FP32); scores, softmax
  *   statistics and accumulators are fp32; outputs are rounded to nearest-even.
  * Supported shapes.  head_dim in {64, 128}; block_size a power of two in [1, 256];
- *   n_q_heads / n_kv_heads in {1, 2, 4, 8}.  Other shapes return PA_EUNSUPPORTED.
+ *   n_q_heads / n_kv_heads in {1, 2, 4, 8, 16}.  Other shapes return PA_EUNSUPPORTED.
  * Errors.  0 = success.  Negative values (PA_E*) mean nothing was launched, except PA_ECUDA,
  *   which reports a launch failure (pa_last_cuda_error() gives the cudaError_t).  Device code never
  *   traps: an out-of-range block id, slot or copy pair met on the device is skipped (treated as

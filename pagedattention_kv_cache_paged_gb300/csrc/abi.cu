@@ -83,7 +83,7 @@ int check_heads(int n_q_heads, int n_kv_heads, int head_dim) {
   if (n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return PA_EINVAL;
   if (n_q_heads % n_kv_heads != 0) return PA_EINVAL;
   const int g = n_q_heads / n_kv_heads;
-  if (g != 1 && g != 2 && g != 4 && g != 8) return PA_EUNSUPPORTED;
+  if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return PA_EUNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PA_EUNSUPPORTED;
   return PA_OK;
 }
@@ -356,7 +356,8 @@ static int decode_impl(void* out, const void* q, const void* k_pool, const void*
   WsLayout ws = workspace_layout(batch, (int64_t)batch * n_q_heads, max_parts, head_dim);
   // up to 8 partitions per row on the tensor-core path: one thread-block cluster per row merges
   // through distributed shared memory, with neither workspace nor merge kernel
-  const bool cluster = use_tc && max_parts >= 2 && max_parts <= 8 && g_options[PA_OPT_CLUSTER_MERGE].load() != 0;
+  const bool cluster = use_tc && max_parts >= 2 && max_parts <= 8 && n_q_heads / n_kv_heads <= 8 &&
+                       g_options[PA_OPT_CLUSTER_MERGE].load() != 0;
   if (max_parts > 1 && !cluster) {
     if (workspace == nullptr) {
       max_parts = 1;

@@ -267,6 +267,7 @@ static cudaError_t launch_simt_g(const AttnArgs& a, cudaStream_t s) {
     case 2: attn_simt_kernel<T, D, 2><<<(unsigned)grid, blk, 0, s>>>(a); break;
     case 4: attn_simt_kernel<T, D, 4><<<(unsigned)grid, blk, 0, s>>>(a); break;
     case 8: attn_simt_kernel<T, D, 8><<<(unsigned)grid, blk, 0, s>>>(a); break;
+    case 16: attn_simt_kernel<T, D, 16><<<(unsigned)grid, blk, 0, s>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

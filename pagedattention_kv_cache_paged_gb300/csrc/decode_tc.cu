@@ -83,21 +83,29 @@ struct TcCfg {
   static_assert(kTcWarps * kStages * 8 <= 1024, "barriers must fit their 1 KB slot");
 };
 
-// Q fragments of the mma A operand for the query group of KV head kvh in sequence b: rows = query
-// heads, two b32 (4 elements) per k-step per lane; rows >= G are zero.
+// Rows of the mma tile that hold query heads: head g in row g, and for groups of 16 head g + 8 in
+// row g + 8 (the second row half of the m16n8k16 tile).
+template <int G>
+struct RowHalves {
+  static constexpr int kN = G > 8 ? 2 : 1;
+};
+
+// Q fragments of the mma A operand for the query group of KV head kvh in sequence b: per k-step,
+// [0] rows g / cols 2*tig, [1] rows g + 8 / cols 2*tig, [2] rows g / cols 8 + 2*tig, [3] rows
+// g + 8 / cols 8 + 2*tig (two elements each).  Rows without a head are zero.
 template <typename T, int D, int G>
 __device__ __forceinline__ void load_q_frags(const AttnArgs& a, int64_t b, int kvh, int lane,
-                                             uint32_t (&qa)[D / 16][2]) {
+                                             uint32_t (&qa)[D / 16][4]) {
   const int g = lane >> 2, tig = lane & 3;
   const T* qrow = static_cast<const T*>(a.q) + (b * a.n_q_heads + (int64_t)kvh * G + g) * D;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    if (g < G) {
-      qa[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig));
-      qa[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig));
-    } else {
-      qa[ks][0] = 0u;
-      qa[ks][1] = 0u;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int head = g + 8 * hh;
+      const bool have = (G > 8 || hh == 0) && head < G;
+      qa[ks][hh] = have ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 8 * hh * D + ks * 16 + 2 * tig)) : 0u;
+      qa[ks][2 + hh] = have ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 8 * hh * D + ks * 16 + 8 + 2 * tig)) : 0u;
     }
   }
 }
@@ -121,16 +129,17 @@ __device__ __forceinline__ void patch_new_token(uint8_t* st, int r, const T* k_s
 }
 
 // Folds one 16-token K/V tile (at st, in the swizzled TMA layout) into the warp's online-softmax
-// state (o, m_run, l_run; rows = query heads in the mma layout).  Tokens >= valid are masked and
-// their V rows zeroed first.
-template <typename T, int D>
-__device__ __forceinline__ void tile_update(uint8_t* st, int valid, const uint32_t (&qa)[D / 16][2],
-                                            float (&o)[D / 8][4], float& m_run, float& l_run, float scale_log2,
-                                            int lane) {
+// state (o, m_run, l_run; rows = query heads in the mma layout, one state per row half).  Tokens
+// >= valid are masked and their V rows zeroed first.
+template <typename T, int D, int G>
+__device__ __forceinline__ void tile_update(uint8_t* st, int valid, const uint32_t (&qa)[D / 16][4],
+                                            float (&o)[D / 8][4], float (&m_run)[2], float (&l_run)[2],
+                                            float scale_log2, int lane) {
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr int kHalves = D / 64;
   constexpr int kKSteps = D / 16;
   constexpr int kDTiles = D / 8;
+  constexpr int kRows = RowHalves<G>::kN;
   const int tig = lane & 3;
   const uint32_t k_base = smem_u32(st);
   const uint32_t v_base = smem_u32(st + kHalves * kHalfBytes);
@@ -157,40 +166,44 @@ __device__ __forceinline__ void tile_update(uint8_t* st, int valid, const uint32
       const uint32_t addr = k_base + (chunk >> 3) * kHalfBytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
       uint32_t b0, b1, b2, b3;
       ldsm_x4(addr, b0, b1, b2, b3);
-      mma_16816<kBf16>(sc[nt], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
-      mma_16816<kBf16>(sc[nt], qa[ks + 1][0], 0u, qa[ks + 1][1], 0u, b2, b3);
+      mma_16816<kBf16>(sc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+      mma_16816<kBf16>(sc[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
     }
   }
-  // ---- online softmax over the tile (rows g, columns = tokens) -----------------------------------
-  float x[4];
+  // ---- online softmax over the tile, per row half (rows g, then g + 8; columns = tokens) ---------
+  uint32_t pa[4] = {0u, 0u, 0u, 0u};  // P as the A operand of P V: [0]/[2] rows g, [1]/[3] rows g + 8
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
+  for (int hh = 0; hh < kRows; ++hh) {
+    float x[4];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int tok = nt * 8 + 2 * tig + e;
-      x[nt * 2 + e] = tok < valid ? sc[nt][e] * scale_log2 : -INFINITY;
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = nt * 8 + 2 * tig + e;
+        x[nt * 2 + e] = tok < valid ? sc[nt][2 * hh + e] * scale_log2 : -INFINITY;
+      }
     }
-  }
-  float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-  tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-  tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-  const float m_new = fmaxf(m_run, tmax);
-  const float corr = fast_exp2(m_run - m_new);
-  float p[4];
+    float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+    const float m_new = fmaxf(m_run[hh], tmax);
+    const float corr = fast_exp2(m_run[hh] - m_new);
+    float p[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - m_new);
-  l_run = l_run * corr + ((p[0] + p[1]) + (p[2] + p[3]));
-  if (__any_sync(0xffffffffu, corr != 1.f)) {
+    for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - m_new);
+    l_run[hh] = l_run[hh] * corr + ((p[0] + p[1]) + (p[2] + p[3]));
+    if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
-    for (int i = 0; i < kDTiles; ++i) {
-      o[i][0] *= corr;
-      o[i][1] *= corr;
+      for (int i = 0; i < kDTiles; ++i) {
+        o[i][2 * hh] *= corr;
+        o[i][2 * hh + 1] *= corr;
+      }
     }
+    m_run[hh] = m_new;
+    pa[hh] = pack2<kBf16>(p[0], p[1]);
+    pa[2 + hh] = pack2<kBf16>(p[2], p[3]);
   }
-  m_run = m_new;
   // ---- O += P V: P from the score registers, V^T fragments by ldmatrix.trans ---------------------
-  const uint32_t pa0 = pack2<kBf16>(p[0], p[1]);
-  const uint32_t pa2 = pack2<kBf16>(p[2], p[3]);
 #pragma unroll
   for (int dt = 0; dt < kDTiles; dt += 2) {
     const int mi = lane >> 3;
@@ -199,13 +212,13 @@ __device__ __forceinline__ void tile_update(uint8_t* st, int valid, const uint32
     const uint32_t addr = v_base + (chunk >> 3) * kHalfBytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
     uint32_t b0, b1, b2, b3;
     ldsm_x4_t(addr, b0, b1, b2, b3);
-    mma_16816<kBf16>(o[dt], pa0, 0u, pa2, 0u, b0, b1);
-    mma_16816<kBf16>(o[dt + 1], pa0, 0u, pa2, 0u, b2, b3);
+    mma_16816<kBf16>(o[dt], pa[0], pa[1], pa[2], pa[3], b0, b1);
+    mma_16816<kBf16>(o[dt + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
   }
 }
 
 template <typename T, int D, int G, bool kCluster>
-__global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
+__global__ void __launch_bounds__(kTcWarps * 32, G > 8 ? 2 : PA_TC_MIN_CTAS)
     decode_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
   constexpr int kHalves = TcCfg<D>::kHalves;
@@ -213,7 +226,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   constexpr int kStages = TcCfg<D>::kStages;
   constexpr int kKSteps = D / 16;
   constexpr int kDTiles = D / 8;
-  static_assert(G <= 8, "query group must fit the first 8 rows of the mma tile");
+  static_assert(G <= 16, "query group must fit the 16 rows of the mma tile");
+  static_assert(!kCluster || G <= 8, "the cluster merge stages at most 8 heads");
+  constexpr int kRows = RowHalves<G>::kN;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -261,7 +276,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
 #pragma unroll
   for (int j = 0; j < kStages; ++j)
     blk_first[j] = (lane == 0 && tile_t0(j) < max_len) ? tile_block(j) : -1;
-  uint32_t qa[kKSteps][2];
+  uint32_t qa[kKSteps][4];
   load_q_frags<T, D, G>(a, row, kvh, lane, qa);
   if (len < 0 || len > max_len) {
     if (threadIdx.x == 0) raise_error(a.err, PA_DEVERR_CONTEXT_LEN);
@@ -325,7 +340,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   float o[kDTiles][4];
 #pragma unroll
   for (int i = 0; i < kDTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   bool timed_out = false;
 
   int j_fail = my_tiles;  // first tile whose wait gave up
@@ -350,7 +365,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
                               static_cast<const T*>(a.v_new) + src_off, static_cast<T*>(a.k_pool_w) + dst_off,
                               static_cast<T*>(a.v_pool_w) + dst_off, lane);
       }
-      tile_update<T, D>(st, valid, qa, o, m_run, l_run, a.scale_log2, lane);
+      tile_update<T, D, G>(st, valid, qa, o, m_run, l_run, a.scale_log2, lane);
     }
     // release the stage and refill it with this warp's tile j + kStages
     fence_proxy_async_smem();
@@ -365,20 +380,25 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   }
   __syncwarp();
 
-  // ---- combine: quad-reduce l, stage (m, l, o) per warp in the warp's own stage 0 --------------
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  // ---- combine: quad-reduce l, stage (m, l, o) per warp in the warp's own stages ----------------
   __syncwarp();
   float* wo = reinterpret_cast<float*>(my_stages);  // [G][D] floats, then m[G], l[G]
-  if (g < G) {
 #pragma unroll
-    for (int i = 0; i < kDTiles; ++i) {
-      wo[g * D + i * 8 + 2 * tig] = o[i][0];
-      wo[g * D + i * 8 + 2 * tig + 1] = o[i][1];
-    }
-    if (tig == 0) {
-      wo[G * D + g] = m_run;
-      wo[G * D + G + g] = my_tiles > 0 && !timed_out ? l_run : 0.f;
+  for (int hh = 0; hh < kRows; ++hh) {
+    float lr = l_run[hh];
+    lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+    lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+    const int gr = g + 8 * hh;  // query head of this row
+    if (gr < G) {
+#pragma unroll
+      for (int i = 0; i < kDTiles; ++i) {
+        wo[gr * D + i * 8 + 2 * tig] = o[i][2 * hh];
+        wo[gr * D + i * 8 + 2 * tig + 1] = o[i][2 * hh + 1];
+      }
+      if (tig == 0) {
+        wo[G * D + gr] = m_run[hh];
+        wo[G * D + G + gr] = my_tiles > 0 && !timed_out ? lr : 0.f;
+      }
     }
   }
   __syncthreads();
@@ -478,7 +498,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
 // kernel.  A sequence of t tiles meets at most ceil(t / per) + 1 <= slots ranges.
 // ------------------------------------------------------------------------------------------------
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
+__global__ void __launch_bounds__(kTcWarps * 32, G > 8 ? 2 : PA_TC_MIN_CTAS)
     decode_bal_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap) {
   constexpr int kHalves = TcCfg<D>::kHalves;
@@ -486,7 +506,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
   constexpr int kStages = TcCfg<D>::kStages;
   constexpr int kKSteps = D / 16;
   constexpr int kDTiles = D / 8;
-  static_assert(G <= 8, "query group must fit the first 8 rows of the mma tile");
+  static_assert(G <= 16, "query group must fit the 16 rows of the mma tile");
+  constexpr int kRows = RowHalves<G>::kN;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -637,12 +658,12 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
           raise_error(a.err, PA_DEVERR_SLOT);
       }
     }
-    uint32_t qa[kKSteps][2];
+    uint32_t qa[kKSteps][4];
     load_q_frags<T, D, G>(a, b, kvh, lane, qa);
     float o[kDTiles][4];
 #pragma unroll
     for (int i = 0; i < kDTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     bool have = false;
     for (int64_t u = g0; u < g1; ++u, ++k) {
       if (k_fail >= 0) continue;
@@ -663,7 +684,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
                                 static_cast<const T*>(a.v_new) + src_off, static_cast<T*>(a.k_pool_w) + dst_off,
                                 static_cast<T*>(a.v_pool_w) + dst_off, lane);
         }
-        tile_update<T, D>(st, valid, qa, o, m_run, l_run, a.scale_log2, lane);
+        tile_update<T, D, G>(st, valid, qa, o, m_run, l_run, a.scale_log2, lane);
         have = true;
       }
       // release the stage and refill it with the range's tile k + kStages
@@ -671,32 +692,37 @@ __global__ void __launch_bounds__(kTcWarps * 32, PA_TC_MIN_CTAS)
       __syncwarp();
       if (lane == 0 && k + kStages < my_tiles) issue(k + kStages);
     }
-    // ---- segment end: output or partial state of rows g < G (query heads of this KV head) --------
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-    const float l_out = have && k_fail < 0 ? l_run : 0.f;
+    // ---- segment end: output or partial state of the rows holding query heads ---------------------
     const bool whole = g0 == ob && g1 == ob + nt;
     const int64_t q_first = ob / per;
-    if (g < G) {
-      const int64_t qh = (int64_t)b * a.n_q_heads + (int64_t)kvh * G + g;
-      if (whole) {
-        const float inv = l_out != 0.f ? 1.f / l_out : 0.f;
-        T* orow = static_cast<T*>(a.out) + qh * D;
 #pragma unroll
-        for (int i = 0; i < kDTiles; ++i) {
-          T* dst = orow + i * 8 + 2 * tig;
-          dst[0] = Elt<T>::from_float(o[i][0] * inv);
-          dst[1] = Elt<T>::from_float(o[i][1] * inv);
-        }
-      } else {
-        const int64_t pi = qh * a.max_parts + (q_unit - q_first);
-        float* acc = a.ws_acc + pi * D;
+    for (int hh = 0; hh < kRows; ++hh) {
+      float lr = l_run[hh];
+      lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+      lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+      const float l_out = have && k_fail < 0 ? lr : 0.f;
+      const int gr = g + 8 * hh;  // query head of this row
+      if (gr < G) {
+        const int64_t qh = (int64_t)b * a.n_q_heads + (int64_t)kvh * G + gr;
+        if (whole) {
+          const float inv = l_out != 0.f ? 1.f / l_out : 0.f;
+          T* orow = static_cast<T*>(a.out) + qh * D;
 #pragma unroll
-        for (int i = 0; i < kDTiles; ++i)
-          *reinterpret_cast<float2*>(acc + i * 8 + 2 * tig) = make_float2(o[i][0], o[i][1]);
-        if (tig == 0) {
-          a.ws_m[pi] = m_run;
-          a.ws_l[pi] = l_out;
+          for (int i = 0; i < kDTiles; ++i) {
+            T* dst = orow + i * 8 + 2 * tig;
+            dst[0] = Elt<T>::from_float(o[i][2 * hh] * inv);
+            dst[1] = Elt<T>::from_float(o[i][2 * hh + 1] * inv);
+          }
+        } else {
+          const int64_t pi = qh * a.max_parts + (q_unit - q_first);
+          float* acc = a.ws_acc + pi * D;
+#pragma unroll
+          for (int i = 0; i < kDTiles; ++i)
+            *reinterpret_cast<float2*>(acc + i * 8 + 2 * tig) = make_float2(o[i][2 * hh], o[i][2 * hh + 1]);
+          if (tig == 0) {
+            a.ws_m[pi] = m_run[hh];
+            a.ws_l[pi] = l_out;
+          }
         }
       }
     }
@@ -770,7 +796,7 @@ bool decode_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, i
   if (dt != PA_BF16 && dt != PA_FP16) return false;
   if (block_size % kTile != 0) return false;
   if (head_dim != 64 && head_dim != 128) return false;
-  if (group > 8) return false;
+  if (group > 16) return false;
   if (num_blocks >= (int64_t(1) << 31)) return false;  // TMA block coordinate is int32
   return encode_fn() != nullptr;
 }
@@ -824,6 +850,7 @@ static cudaError_t launch_tc_d(const AttnArgs& a, const CUtensorMap& km, const C
     case 2: return launch_tc_c<T, D, 2>(a, km, vm, s);
     case 4: return launch_tc_c<T, D, 4>(a, km, vm, s);
     case 8: return launch_tc_c<T, D, 8>(a, km, vm, s);
+    case 16: return launch_tc_g<T, D, 16, false>(a, km, vm, s);  // no cluster merge for 16 heads
     default: return cudaErrorInvalidValue;
   }
 }
@@ -892,6 +919,7 @@ static cudaError_t launch_bal_d(const AttnArgs& a, const CUtensorMap& km, const 
     case 2: return launch_bal_g<T, D, 2>(a, km, vm, s);
     case 4: return launch_bal_g<T, D, 4>(a, km, vm, s);
     case 8: return launch_bal_g<T, D, 8>(a, km, vm, s);
+    case 16: return launch_bal_g<T, D, 16>(a, km, vm, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -412,6 +412,7 @@ static cudaError_t launch_pf_d(const AttnArgs& a, const CUtensorMap& km, const C
     case 2: return launch_pf_g<T, D, 2>(a, km, vm, s);
     case 4: return launch_pf_g<T, D, 4>(a, km, vm, s);
     case 8: return launch_pf_g<T, D, 8>(a, km, vm, s);
+    case 16: return launch_pf_g<T, D, 16>(a, km, vm, s);
     default: return cudaErrorInvalidValue;
   }
 }

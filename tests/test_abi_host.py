@@ -86,7 +86,8 @@ def test_argument_errors_are_returned_before_any_launch(lib):
     # heads not divisible / unsupported group / unsupported head_dim / bad block size
     args = [n, n, n, n, n, 4, n, 2, 8, 16, 1.0]
     assert lib.paged_attention_decode(*args, 6, 4, 64, pa.PA_BF16, n, 0, n) == pa.PA_EINVAL
-    assert lib.paged_attention_decode(*args, 48, 3, 64, pa.PA_BF16, n, 0, n) == pa.PA_EUNSUPPORTED
+    assert lib.paged_attention_decode(*args, 96, 3, 64, pa.PA_BF16, n, 0, n) == pa.PA_EUNSUPPORTED  # group 32
+    assert lib.paged_attention_decode(*args, 36, 3, 64, pa.PA_BF16, n, 0, n) == pa.PA_EUNSUPPORTED  # group 12
     assert lib.paged_attention_decode(*args, 8, 2, 96, pa.PA_BF16, n, 0, n) == pa.PA_EUNSUPPORTED
     bad_bs = [n, n, n, n, n, 4, n, 2, 8, 12, 1.0]
     assert lib.paged_attention_decode(*bad_bs, 8, 2, 64, pa.PA_BF16, n, 0, n) == pa.PA_EUNSUPPORTED

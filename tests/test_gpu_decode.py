@@ -216,7 +216,7 @@ def test_decode_grids_on_a_ragged_batch_with_empty_sequences(cuda_lib, dtype, gr
     assert pa.device_error_flags() == 0
 
 
-@pytest.mark.parametrize("G,D", [(1, 64), (2, 128), (4, 128), (8, 128), (8, 64)])
+@pytest.mark.parametrize("G,D", [(1, 64), (2, 128), (4, 128), (8, 128), (8, 64), (16, 128), (16, 64)])
 def test_equal_work_grid_other_groups_and_head_dims(cuda_lib, G, D):
     """The equal-work grid for every query-group size and head_dim."""
     pa = cuda_lib
@@ -250,6 +250,30 @@ def test_split_decode_is_deterministic_and_stale_workspace_safe(cuda_lib, grid):
     out2 = run_decode(pa, case, lens=lens, workspace=ws).cpu()
     assert torch.equal(bits(out1), bits(out2))
     assert torch.isfinite(out1.float()).all()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("part", [0, 64, "none"])
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_decode_group_of_16_query_heads(cuda_lib, dtype, D, part, kernel):
+    """16 query heads per KV head: both row halves of the tensor-core kernel's mma tile hold
+    heads (and the CUDA-core path, kernel 1 or fp32, its largest query group)."""
+    pa = cuda_lib
+    pa.set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
+    ws = None
+    if part != "none":
+        pa.set_option(pa.PA_OPT_PARTITION_TOKENS, part)
+        ws = "auto"
+    lens = [0, 1, 15, 16, 17, 200, 517, 1300]
+    case = _ragged_case(dtype, 32, 2, D, 16, lens, seed=D + 16)
+    dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
+    pa.paged_kv_write(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), dk, dv)
+    out = run_decode(pa, case, kp=dk, vp=dv, workspace=ws)
+    kp1, vp1 = oracle.paged_kv_write(case.k_pool, case.v_pool, case.k_new, case.v_new, case.slot_mapping)
+    ref = oracle.paged_decode(case.q, kp1, vp1, case.block_table, case.context_lens, case.scale)
+    assert_close(out, ref, dtype, f"G16 {dtype} D{D} part{part} kernel{kernel}")
+    assert pa.device_error_flags() == 0
 
 
 @pytest.mark.parametrize("dtype", DTYPES)

@@ -50,7 +50,7 @@ def _both(pa, case, workspace="auto"):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("D,G,S", [(128, 4, 16), (64, 1, 16), (128, 8, 32), (64, 2, 8)])
+@pytest.mark.parametrize("D,G,S", [(128, 4, 16), (64, 1, 16), (128, 8, 32), (64, 2, 8), (128, 16, 16)])
 @pytest.mark.parametrize("kernel", [0, 1])
 @pytest.mark.parametrize("split", [True, False, "cluster", "equal-work"])
 def test_fused_equals_write_then_decode(cuda_lib, dtype, D, G, S, kernel, split):

@@ -54,7 +54,7 @@ def oracle_pools(case):
 
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("G", [1, 4, 8, 16])
 @pytest.mark.parametrize("S", [16, 32])
 @pytest.mark.parametrize("kernel", [0, 1, 3])
 def test_prefill_ragged_chunks(cuda_lib, dtype, D, G, S, kernel):
