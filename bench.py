@@ -161,7 +161,10 @@ def cpu_baseline(budget_s: float = 10.0):
     until about ``budget_s`` seconds of oracle time are spent."""
     import oracle
     lens = W.llama_context_lens()
+    threads = torch.get_num_threads()
+    torch.set_num_threads(1)  # the oracle's torch indexing on one core, like its numpy arithmetic
     done_bytes, spent, seqs, tokens = 0, 0.0, 0, 0
+    g_bytes, g_spent = 0, 0.0
     while spent < budget_s and seqs < 512:
         n = lens[seqs % len(lens)]
         case = W.decode_case("cpu_sample", W.SEED_BASE + 3 + 17 * seqs, [n - 1], n_q_heads=HQ, n_kv_heads=HKV,
@@ -171,13 +174,24 @@ def cpu_baseline(budget_s: float = 10.0):
         kp, vp = oracle.paged_kv_write(case.k_pool, case.v_pool, case.k_new, case.v_new, case.slot_mapping)
         oracle.paged_decode(case.q, kp, vp, case.block_table, case.context_lens, case.scale)
         spent += time.perf_counter() - t0
+        # the gather alone: the contiguous copy of K and V through the block table that a fused
+        # paged read avoids
+        t1 = time.perf_counter()
+        oracle.gather_history(kp, case.block_table[0], n, S)
+        oracle.gather_history(vp, case.block_table[0], n, S)
+        g_spent += time.perf_counter() - t1
+        g_bytes += n * HKV * D * ELT * 2
         kvb, wb = algorithmic_bytes([n], 1)
         done_bytes += kvb + wb
         tokens += n
         seqs += 1
+    torch.set_num_threads(threads)
     return {"value": done_bytes / spent / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{seqs} sequences of the 64-sequence serving batch, cycled (write + decode, {tokens} "
-                      f"context tokens), {spent:.1f} s of single-threaded numpy fp64"}
+                      f"context tokens), {spent:.1f} s of single-threaded numpy / torch fp64",
+            "gather_only": {"value": g_bytes / g_spent / 1e9, "unit": UNIT,
+                            "what": "the oracle's contiguous gather of each sequence's K and V through its block "
+                                    "table (upcast to fp64), alone: the copy the fused paged read avoids"}}
 
 
 def run_reference(args):
@@ -189,6 +203,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
+    torch.set_num_threads(1)  # one host core, as the line states
     lens = W.llama_context_lens()
     cases = []
     for i in range(8):
