@@ -5,17 +5,20 @@
 // positions of sequence b's context and query r attends to positions 0 .. n_b - m_b + r through
 // the block table — on the 5th-generation tensor cores with accumulators in tensor memory.
 //
-// CTA = 256 (query token, head) rows of one KV head, split into two 128-row Q tiles that share
-// every K/V tile (kRows / G tokens x the G heads of the group: read-time GQA, nanoserve Day 19
-// "What I learned" 4).  11 warps:
+// Persistent: one CTA per SM walks the work items (blockIdx, blockIdx + gridDim, ...).  An item =
+// 256 (query token, head) rows of one KV head, split into two 128-row Q tiles that share every K/V
+// tile (kRows / G tokens x the G heads of the group: read-time GQA, nanoserve Day 19 "What I
+// learned" 4).  11 warps:
 //   warps 0-3 / 4-7  softmax groups 0 / 1: thread t of group k owns row 128k + t (TMEM lane t of
 //              S_k and O_k); turns each S_k tile into probabilities, rescales O_k in TMEM only when
 //              its stabilising maximum has to move up by more than 2^8, writes P_k (bf16/fp16) back
 //              into the TMEM columns of S_k, and normalises O_k at the end;
-//   warp 8     K producer: loads both Q tiles (one TMA box per 64-column half), then streams 128-key
-//              K tiles (TMA boxes of 16 keys x 64 columns from the physical blocks the table names)
-//              into a 3-stage ring and publishes which sub-tiles hold data;
-//   warp 9     V producer: the matching V tiles into a 2-stage ring;
+//   warp 8     K producer: streams 128-key K tiles (TMA boxes of 16 keys x 64 columns from the
+//              physical blocks the table names) into a kUmKStages-deep ring and publishes which
+//              sub-tiles hold data;
+//   warp 9     V producer: each item's two Q tiles (one TMA box per 64-column half, once the
+//              previous item's S products are done), then the matching V tiles into a
+//              kUmVStages-deep ring;
 //   warp 10    MMA: allocates TMEM (S_0, S_1: 128 columns each; O_0, O_1: 128 columns each) and
 //              issues S_k = Q_k K^T (M 128, N 128, both operands in shared memory) and
 //              O_k += P_k V (M 128, N head_dim, P read from TMEM, V an MN-major shared-memory
@@ -44,8 +47,16 @@ constexpr int kUmRows = 2 * kUmTileRows;    // rows per CTA
 constexpr int kUmKeys = 128;                // keys per K/V tile (N of S, K of PV)
 constexpr int kUmSub = kUmKeys / 16;
 constexpr int kUmTmemCols = 512;
-constexpr int kUmKStages = 3;               // K ring depth
-constexpr int kUmVStages = 2;               // V ring depth
+// Ring depths (build-time overridable): K 2 / V 3 measured 1 % faster than K 3 / V 2 (V tiles are
+// needed later in a tile's chain, so their loads profit from the deeper ring)
+#ifndef PA_UM_KSTAGES
+#define PA_UM_KSTAGES 2
+#endif
+#ifndef PA_UM_VSTAGES
+#define PA_UM_VSTAGES 3
+#endif
+constexpr int kUmKStages = PA_UM_KSTAGES;   // K ring depth
+constexpr int kUmVStages = PA_UM_VSTAGES;   // V ring depth
 constexpr float kUmRescaleThreshold = 8.f;  // log2 units: O is rescaled when the max grows by > 2^8
 // 1: one CTA per SM walking the work items; 0: one CTA per work item
 #ifndef PA_UM_PERSISTENT
