@@ -42,9 +42,9 @@ ELT = 2  # bf16
 # metrics.  Retake it whenever either kernel changes.
 FUSED_CALL_DRAM_BYTES = 585.9e6
 # dram__bytes_read.sum + dram__bytes_write.sum of one tcgen05 prefill launch on the chunked-prefill
-# workload (554.7 + 237.0 MB), from one `ncu --set full` capture of the persistent kernel.  Retake it
-# whenever the kernel changes.
-PREFILL_DRAM_BYTES = 791.7e6
+# workload (555.2 + 235.7 MB, mean of two launches), from one ncu capture of those metrics on the
+# current kernel (K 2 / V 3 rings).  Retake it whenever the kernel changes.
+PREFILL_DRAM_BYTES = 790.9e6
 
 
 def measured_peaks():
