@@ -39,12 +39,14 @@ ELT = 2  # bf16
 # dram__bytes_read.sum + dram__bytes_write.sum of one paged_attention_decode_fused call on this
 # workload with separate pools and the per-partition grid (partition kernel 578.7 + 2.9 MB, merge
 # kernel 4.3 MB with the cold L2 of the capture; mean of two calls), from one ncu capture of those
-# metrics.  Retake it whenever either kernel changes.
+# metrics on the current kernels (no sleep between barrier polls).  Retake it whenever either
+# kernel changes.
 FUSED_CALL_DRAM_BYTES = 585.9e6
 # dram__bytes_read.sum + dram__bytes_write.sum of one tcgen05 prefill launch on the chunked-prefill
-# workload (555.2 + 235.7 MB, mean of two launches), from one ncu capture of those metrics on the
-# current kernel (K 2 / V 3 rings).  Retake it whenever the kernel changes.
-PREFILL_DRAM_BYTES = 790.9e6
+# workload (554.4 + 235.2 MB, mean of two launches), from one ncu capture of those metrics on the
+# current kernel (K 2 / V 3 rings, no sleep between barrier polls).  Retake it whenever the kernel
+# changes.
+PREFILL_DRAM_BYTES = 789.6e6
 
 
 def measured_peaks():
