@@ -115,6 +115,34 @@ def test_workspace_size_follows_the_partition_plan(lib):
     assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 0) == 0
 
 
+def _expected_workspace(batch, stride, bs, hq, hkv, d, part=0):
+    """The documented split-K plan: automatic partitions give about one wave of 456 decode CTAs when
+    every row is as long as its table allows, clamped to [256, 1024] tokens and rounded up to the
+    block size; slots = partitions + 1; acc, max, sum and per-sequence slot counts, 16-byte aligned."""
+    max_len = stride * bs
+    if part <= 0:
+        part = min(max(-(-batch * hkv * max_len // 456), 256), 1024)
+    part = -(-part // bs) * bs
+    if part >= max_len:
+        return 0
+    slots = -(-max_len // part) + 1
+    n = batch * hq * slots
+    up16 = lambda x: (x + 15) // 16 * 16
+    return n * d * 4 + 2 * up16(n * 4) + up16(batch * 4)
+
+
+@pytest.mark.parametrize("shape", [(64, 256, 16, 32, 8, 128), (1, 128, 16, 12, 12, 64), (8, 128, 16, 12, 12, 64),
+                                   (4, 8192, 16, 32, 8, 128), (64, 8, 16, 32, 8, 128), (3, 40, 32, 16, 1, 64)])
+def test_automatic_split_plan(lib, shape):
+    f = lib.paged_attention_decode_workspace_size
+    assert f(*shape) == _expected_workspace(*shape)
+    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 512) == 0
+    try:
+        assert f(*shape) == _expected_workspace(*shape, part=512)
+    finally:
+        assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 0) == 0
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     kp = torch.zeros((4, 16, 2, 64))
