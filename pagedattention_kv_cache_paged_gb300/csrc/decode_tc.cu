@@ -758,6 +758,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
+// L2 promotion of the pool boxes' reads (build-time overridable: 0 none, 1 64 B, 2 128 B, 3 256 B)
+#ifndef PA_POOL_L2_PROMOTION
+#define PA_POOL_L2_PROMOTION 3
+#endif
+
 // Pool viewed as a 3-D tensor (column in [0, n_kv_heads * head_dim), token in block, block) with the
 // pool's own block stride (so separate pools and unified K/V blocks share one code path); boxes of
 // 64 columns x 16 tokens x 1 block.
@@ -770,8 +775,12 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, pa_dtype dt, int64_t nu
   const cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType ty = dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapL2promotion promo = PA_POOL_L2_PROMOTION == 0   ? CU_TENSOR_MAP_L2_PROMOTION_NONE
+                                       : PA_POOL_L2_PROMOTION == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
+                                       : PA_POOL_L2_PROMOTION == 2 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                                                   : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   CUresult r = fn(map, ty, 3, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

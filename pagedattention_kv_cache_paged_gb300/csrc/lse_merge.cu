@@ -18,7 +18,10 @@
 
 namespace pa {
 
-constexpr int kMergeWarps = 4;
+#ifndef PA_MERGE_WARPS
+#define PA_MERGE_WARPS 4
+#endif
+constexpr int kMergeWarps = PA_MERGE_WARPS;  // rows (warps) per CTA of the one-warp-per-row merge
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const MergeArgs a) {
