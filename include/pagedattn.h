@@ -18,16 +18,17 @@
  *   the device cache tensor is indexed block, token-in-block, kv head, head dim; JuliaPagedAttn
  *   README, "Block Layout": a block holds block_size consecutive tokens for every KV head).
  *   Pool base pointers must be 16-byte aligned.
- * Unified K/V blocks.  With pa_set_option(PA_OPT_KV_LAYOUT, 1) there is one pool
- *   [num_blocks][2][block_size][n_kv_heads][head_dim]: physical block b holds the keys of its
- *   block_size tokens followed by their values, so one table and one allocation serve both
- *   (JuliaPagedAttn README, "Features": unified K/V blocks, keys and values of a token in one
- *   block, a single block table and pool).  Every call keeps its k_pool / v_pool pair: k_pool is
- *   the pool's base and v_pool must be k_pool + block_size * n_kv_heads * head_dim * element size
- *   (the V half of block 0); any other v_pool returns PA_EINVAL.  Slots, tables, block ids and
- *   results are the same as with separate pools; only the distance between consecutive blocks of
- *   the K (or V) view doubles.  The layout is a process-wide setting: change it only between
- *   calls, never while kernels of another layout are in flight on pools the caller reuses.
+ * Block stride and unified K/V blocks.  The calls above take contiguous pools: block b of a pool
+ *   starts b * block bytes after its base (block bytes = block_size * n_kv_heads * head_dim *
+ *   element size).  Each has an `_ex` twin whose optional pa_opts says how far apart the blocks
+ *   of each pool lie (kv_block_stride_bytes), so the same kernels also read pools whose blocks are
+ *   interleaved with other data.  The case the pages name is unified K/V blocks (JuliaPagedAttn
+ *   README, "Features": keys and values of a token in one block, a single block table and pool):
+ *   one pool [num_blocks][2][block_size][n_kv_heads][head_dim] where physical block b holds the
+ *   keys of its block_size tokens followed by their values.  Pass k_pool = the pool's base,
+ *   v_pool = k_pool + block bytes and kv_block_stride_bytes = 2 * block bytes.  Slots, tables,
+ *   block ids and results are the same as with separate pools.  The stride is a per-call argument:
+ *   calls with different layouts may run concurrently from any number of threads.
  * Slots.  Logical position j of sequence b lives in slot
  *   block_table[b * block_table_stride + j / block_size] * block_size + j % block_size,
  *   i.e. row `slot` of the pool viewed as [num_blocks * block_size][n_kv_heads][head_dim].
@@ -46,9 +47,12 @@
  *   which reports a launch failure (pa_last_cuda_error() gives the cudaError_t).  Device code never
  *   traps: an out-of-range block id, slot or copy pair met on the device is skipped (treated as
  *   masked) and recorded in a device error word that pa_device_error_flags() reads back.  With
- *   checked mode on (pa_set_option(PA_OPT_CHECKED, 1)) each call first copies its index arrays to
- *   the host, synchronizing `stream`, and returns PA_ERANGE without launching if any index, length
- *   or duplicate is invalid.
+ *   checked mode on (pa_set_checked_mode(1)) each call first copies its index arrays to the host,
+ *   synchronizing `stream`, and returns PA_ERANGE without launching if any index, length or
+ *   duplicate is invalid.
+ * State.  The library keeps no state that changes what a call computes other than the checked-mode
+ *   flag.  It also holds, per device, the device error word and the address lookups it needs to
+ *   launch (tensor-map encoder, SM count), none of which alters results.
  */
 #ifndef PAGEDATTN_H_
 #define PAGEDATTN_H_
@@ -88,29 +92,33 @@ enum {
   PA_DEVERR_TIMEOUT = 32      /* a bounded wait in a pipelined kernel gave up (the kernel returned early) */
 };
 
-/* Options for pa_set_option / pa_get_option (process-wide). */
+/* Options for pa_set_option / pa_get_option.  The only process-wide option is the checked mode. */
 enum {
-  PA_OPT_CHECKED = 1,          /* 0 (default) or 1: host-side validation before each launch */
-  PA_OPT_DECODE_KERNEL = 2,    /* 0 auto (default), 1 CUDA-core kernel, 2 tensor-core kernel */
-  PA_OPT_PARTITION_TOKENS = 3, /* split-K partition length in tokens, rounded up to block_size; 0 (default)
-                                  = automatic: about one wave of decode CTAs (456) when every row is
-                                  as long as the table allows, clamped to [256, 1024] tokens */
-  PA_OPT_PREFILL_KERNEL = 4,   /* 0 auto (default), 1 CUDA-core kernel, 2 tcgen05 tensor-core kernel,
-                                  3 mma.sync tensor-core kernel */
-  PA_OPT_CLUSTER_MERGE = 5,    /* 0 (default) or 1: on the tensor-core decode path, rows split into 2-8
-                                  partitions merge inside one thread-block cluster (distributed shared
-                                  memory) instead of the workspace + merge kernel.  Off by default: a
-                                  cluster keeps all its CTAs resident until its longest partition ends,
-                                  which cost 20 % at the serving shape */
-  PA_OPT_KV_LAYOUT = 6,        /* pool layout of every call: 0 (default) separate K and V pools (see
-                                  "Pools"); 1 unified K/V blocks (see "Unified K/V blocks") */
-  PA_OPT_DECODE_GRID = 7       /* split-K grid of the tensor-core decode when rows split: 0 (default)
-                                  one CTA per (sequence, KV head, partition_tokens-long partition),
-                                  scheduled by the hardware; 1 equal work per warp (each KV head's
-                                  tiles of all sequences laid end to end and cut into one wave of
-                                  equal ranges).  Measured slower at the serving shape: a static
-                                  split cannot follow the uneven bandwidth the SMs get */
+  PA_OPT_CHECKED = 1           /* 0 (default) or 1: host-side validation before each launch */
 };
+
+/*
+ * Per-call options of the `_ex` entry points.  A NULL pointer, or a zero-filled struct, means the
+ * defaults; nothing here outlives the call.  Invalid values return PA_EINVAL.
+ *   kv_block_stride_bytes  distance between consecutive blocks of each pool, a multiple of 16 and
+ *                          at least the block bytes; 0 = the block bytes (contiguous pools).  See
+ *                          "Block stride and unified K/V blocks".
+ *   decode_kernel          0 auto (tensor cores for bf16/fp16 pools with block_size % 16 == 0, else
+ *                          CUDA cores), 1 CUDA cores, 2 tensor cores (PA_EUNSUPPORTED if the shape
+ *                          does not allow them)
+ *   prefill_kernel         0 auto (tcgen05 tensor cores where the shape allows, else CUDA cores),
+ *                          1 CUDA cores, 2 tcgen05 (PA_EUNSUPPORTED if the shape does not allow it)
+ *   partition_tokens       split-K partition length in tokens, rounded up to block_size, at most
+ *                          2^30; 0 = automatic (see paged_attention_decode_workspace_size)
+ *   reserved               must be 0
+ */
+typedef struct pa_opts {
+  int64_t kv_block_stride_bytes;
+  int32_t decode_kernel;
+  int32_t prefill_kernel;
+  int32_t partition_tokens;
+  int32_t reserved;
+} pa_opts;
 
 /*
  * paged_kv_write — scatter this step's K/V into the pools through slot_mapping.
@@ -127,6 +135,10 @@ enum {
 PA_API int paged_kv_write(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens,
                    void* k_pool, void* v_pool, int64_t num_blocks, int block_size, int n_kv_heads,
                    int head_dim, pa_dtype dtype, void* stream);
+/* paged_kv_write with per-call options (opts may be NULL; only kv_block_stride_bytes applies). */
+PA_API int paged_kv_write_ex(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens,
+                             void* k_pool, void* v_pool, int64_t num_blocks, int block_size, int n_kv_heads,
+                             int head_dim, pa_dtype dtype, const pa_opts* opts, void* stream);
 
 /*
  * paged_attention_decode — one query token per sequence attends over its whole paged context.
@@ -150,6 +162,13 @@ PA_API int paged_attention_decode(void* out, const void* q, const void* k_pool, 
                            const int32_t* context_lens, int batch, int64_t num_blocks, int block_size,
                            float scale, int n_q_heads, int n_kv_heads, int head_dim, pa_dtype dtype,
                            void* workspace, size_t workspace_bytes, void* stream);
+/* paged_attention_decode with per-call options (opts may be NULL).  The workspace must be at least
+ * paged_attention_decode_workspace_size_ex(..., opts) bytes for the same opts. */
+PA_API int paged_attention_decode_ex(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                     const int32_t* block_table, int64_t block_table_stride,
+                                     const int32_t* context_lens, int batch, int64_t num_blocks, int block_size,
+                                     float scale, int n_q_heads, int n_kv_heads, int head_dim, pa_dtype dtype,
+                                     void* workspace, size_t workspace_bytes, const pa_opts* opts, void* stream);
 
 /*
  * paged_attention_decode_fused — paged_kv_write of each sequence's new token followed by
@@ -171,10 +190,36 @@ PA_API int paged_attention_decode_fused(void* out, const void* q, const void* k_
                                         const int32_t* context_lens, int batch, int64_t num_blocks, int block_size,
                                         float scale, int n_q_heads, int n_kv_heads, int head_dim, pa_dtype dtype,
                                         void* workspace, size_t workspace_bytes, void* stream);
+/* paged_attention_decode_fused with per-call options (opts may be NULL). */
+PA_API int paged_attention_decode_fused_ex(void* out, const void* q, const void* k_new, const void* v_new,
+                                           const int64_t* slot_mapping, void* k_pool, void* v_pool,
+                                           const int32_t* block_table, int64_t block_table_stride,
+                                           const int32_t* context_lens, int batch, int64_t num_blocks,
+                                           int block_size, float scale, int n_q_heads, int n_kv_heads, int head_dim,
+                                           pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                                           const pa_opts* opts, void* stream);
 
-/* Workspace bytes paged_attention_decode needs for split-K with these sizes (0 if it never splits). */
+/*
+ * Workspace bytes paged_attention_decode needs for split-K with these sizes on the current device
+ * (0 if it never splits).  The split-K plan: a row (sequence, KV head) as long as its table allows
+ * is cut into partitions of P tokens, P chosen so that the grid holds about one wave of decode
+ * CTAs on this device (its SM count x 3 resident CTAs, x 2 for groups of 16 query heads), clamped
+ * to [256, 1024] tokens and rounded up to block_size; rows no longer than P are not split.  The
+ * `_ex` form applies opts->partition_tokens instead when it is non-zero.  Invalid sizes give 0.
+ */
 PA_API size_t paged_attention_decode_workspace_size(int batch, int64_t block_table_stride, int block_size,
                                              int n_q_heads, int n_kv_heads, int head_dim);
+PA_API size_t paged_attention_decode_workspace_size_ex(int batch, int64_t block_table_stride, int block_size,
+                                                       int n_q_heads, int n_kv_heads, int head_dim,
+                                                       const pa_opts* opts);
+
+/* The split-K plan above for a device with sm_count SMs, computed on the host without touching a
+ * device: *part_tokens (partition length), *max_parts (partitions of a row as long as its table
+ * allows; 1 = no split) and *workspace_bytes.  partition_tokens as in pa_opts (0 = automatic).
+ * Returns PA_EINVAL for invalid sizes or a null output pointer. */
+PA_API int pa_decode_split_plan(int batch, int64_t block_table_stride, int block_size, int n_q_heads, int n_kv_heads,
+                                int head_dim, int partition_tokens, int sm_count, int* part_tokens, int* max_parts,
+                                size_t* workspace_bytes);
 
 /*
  * paged_attention_prefill — causal chunked prefill over a paged history.
@@ -193,6 +238,13 @@ PA_API int paged_attention_prefill(void* out, const void* q, const int32_t* quer
                             int64_t block_table_stride, const int32_t* context_lens, int batch,
                             int64_t num_blocks, int block_size, float scale, int n_q_heads,
                             int n_kv_heads, int head_dim, pa_dtype dtype, void* stream);
+/* paged_attention_prefill with per-call options (opts may be NULL). */
+PA_API int paged_attention_prefill_ex(void* out, const void* q, const int32_t* query_start_loc, int64_t total_q,
+                                      const void* k_pool, const void* v_pool, const int32_t* block_table,
+                                      int64_t block_table_stride, const int32_t* context_lens, int batch,
+                                      int64_t num_blocks, int block_size, float scale, int n_q_heads,
+                                      int n_kv_heads, int head_dim, pa_dtype dtype, const pa_opts* opts,
+                                      void* stream);
 
 /*
  * copy_blocks — make physical block dst a bit copy of block src, in both pools, for each pair.
@@ -201,11 +253,13 @@ PA_API int paged_attention_prefill(void* out, const void* q, const int32_t* quer
  * "cow_fork!".
  *   block_pairs  int64 [n_pairs][2] = (src, dst).  A dst must not appear twice nor as a src of
  *                another pair (checked mode rejects both); block_bytes = block_size * n_kv_heads *
- *                head_dim * element size, a multiple of 16 (the bytes of one K half; with unified
- *                K/V blocks v_pool = k_pool + block_bytes and blocks lie 2 * block_bytes apart).
+ *                head_dim * element size, a multiple of 16 (the bytes of one block of one pool).
  */
 PA_API int copy_blocks(void* k_pool, void* v_pool, const int64_t* block_pairs, int64_t n_pairs,
                 int64_t num_blocks, int64_t block_bytes, void* stream);
+/* copy_blocks with per-call options (opts may be NULL; only kv_block_stride_bytes applies). */
+PA_API int copy_blocks_ex(void* k_pool, void* v_pool, const int64_t* block_pairs, int64_t n_pairs,
+                          int64_t num_blocks, int64_t block_bytes, const pa_opts* opts, void* stream);
 
 /*
  * swap_blocks — move blocks between two pools in one launch: the device pool and a pinned host pool
@@ -220,13 +274,17 @@ PA_API int copy_blocks(void* k_pool, void* v_pool, const int64_t* block_pairs, i
  *                A dst must not appear twice (checked mode rejects it); out-of-range ids are
  *                skipped on the device and recorded as PA_DEVERR_COPY_PAIR.
  *   block_bytes  bytes of one block of one pool (block_size * n_kv_heads * head_dim * element size),
- *                a multiple of 16.  With unified K/V blocks both sides use that layout: each
- *                v pointer = its k pointer + block_bytes.  The copy is bit-exact and ordered on
- *                `stream`.
+ *                a multiple of 16.  The copy is bit-exact and ordered on `stream`.
  */
 PA_API int swap_blocks(void* dst_k_pool, void* dst_v_pool, int64_t dst_num_blocks, const void* src_k_pool,
                        const void* src_v_pool, int64_t src_num_blocks, const int64_t* block_pairs, int64_t n_pairs,
                        int64_t block_bytes, void* stream);
+/* swap_blocks with per-call options (opts may be NULL; only kv_block_stride_bytes applies, to both
+ * sides: for unified K/V blocks on both sides pass each v pointer = its k pointer + block_bytes
+ * and kv_block_stride_bytes = 2 * block_bytes). */
+PA_API int swap_blocks_ex(void* dst_k_pool, void* dst_v_pool, int64_t dst_num_blocks, const void* src_k_pool,
+                          const void* src_v_pool, int64_t src_num_blocks, const int64_t* block_pairs,
+                          int64_t n_pairs, int64_t block_bytes, const pa_opts* opts, void* stream);
 
 /*
  * paged_attention_lse_merge — merge split-K partials exactly (the partition-combining identity of
@@ -252,14 +310,17 @@ PA_API int paged_attention_lse_merge(void* out, const float* part_max, const flo
  * the hot path (cudaMalloc may synchronize the device), or a foreign-language caller that only
  * holds raw device pointers.  Such callers cannot provide the split-K workspace.
  *
- * Arguments and results are exactly those of paged_attention_decode without the workspace pair.
- * The split-K scratch lives instead in a file-scope device array of PA_STATIC_SCRATCH_BYTES that
- * every GPU loading this library holds until the process exits.  No call allocates or frees
- * anything.
- *   - The first call on a device looks up the array's device address with that device current (a
- *     one-time host set-up); make that first call before any stream capture.
- *   - Problems whose split-K scratch (paged_attention_decode_workspace_size) exceeds
- *     PA_STATIC_SCRATCH_BYTES are rejected with PA_EWORKSPACE before anything is launched.
+ * Arguments and results are exactly those of paged_attention_decode without the workspace pair
+ * (contiguous pools, default options); the output is bit-identical to paged_attention_decode with
+ * a caller workspace.  The split-K scratch lives instead in a file-scope device array of
+ * PA_STATIC_SCRATCH_BYTES that every GPU loading this library holds until the process exits.  No
+ * call allocates or frees anything.
+ *   - The first call on a device (in each CUDA context: again after a device reset) looks up the
+ *     array's device address with that device current, a one-time host set-up; make that first
+ *     call before any stream capture.
+ *   - Arguments are validated first, exactly as by paged_attention_decode; then problems whose
+ *     split-K scratch (paged_attention_decode_workspace_size) exceeds PA_STATIC_SCRATCH_BYTES are
+ *     rejected with PA_EWORKSPACE before anything is launched.
  *   - All calls on a device share the one array and it keeps the last call's contents; nothing in
  *     it needs to start at zero.  Calls whose kernels overlap on the GPU (other streams, other
  *     threads) race on the array: serialize them on one stream.
@@ -271,8 +332,10 @@ PA_API int paged_attention_decode_static_scratch(void* out, const void* q, const
                                                  int block_size, float scale, int n_q_heads, int n_kv_heads,
                                                  int head_dim, pa_dtype dtype, void* stream);
 
-/* Set / get a process-wide option (PA_OPT_*).  pa_set_option returns PA_EINVAL for an unknown option
- * or a bad value. */
+/* Checked mode on (1) or off (0, the default): the library's one process-wide setting.
+ * pa_set_checked_mode(on) is pa_set_option(PA_OPT_CHECKED, on); any other option or value returns
+ * PA_EINVAL, and pa_get_option of an unknown option returns PA_EINVAL. */
+PA_API int pa_set_checked_mode(int on);
 PA_API int pa_set_option(int option, int64_t value);
 PA_API int64_t pa_get_option(int option);
 
@@ -283,21 +346,27 @@ PA_API int pa_last_cuda_error(void);
 PA_API const char* pa_status_string(int status);
 
 /* Read (and, if clear != 0, reset) the device error word of the current device.  Synchronizes
- * `stream`.  Returns the PA_DEVERR_* bits, or a negative status on a CUDA failure. */
+ * `stream`.  Returns the PA_DEVERR_* bits, or a negative status on a CUDA failure.  The word
+ * accumulates over launches until cleared; clearing is only for reporting: a timeout recorded by one
+ * launch never shortens the waits of a later one (see pa_selftest_bounded_wait). */
 PA_API int pa_device_error_flags(int clear, void* stream);
 
 /*
  * pa_selftest_bounded_wait — run the failure path of the library's bounded waits on the device.
  * The pages have no counterpart: this is a test hook for the library itself.  Every pipelined kernel
  * (TMA rings, tensor-memory hand-offs) waits on mbarriers with a time limit and, when one runs out,
- * records PA_DEVERR_TIMEOUT and returns instead of hanging; the other waiting warps and CTAs see
- * that bit and leave too.  This call launches one CTA that does exactly that on barriers nothing
- * completes: warp 0 gives up after limit_ns and sets the bit, warp 1 (limit 1 s) must leave as soon
- * as it sees it.  Nothing faults and the context stays usable.
+ * records PA_DEVERR_TIMEOUT and returns instead of hanging; the other waiting warps and CTAs of
+ * the same launch see that and leave too.  The abort is scoped to the launch: each launch carries
+ * its own epoch number and a wait leaves early only when the launch that gave up was its own, so a
+ * later, healthy launch runs to completion even while PA_DEVERR_TIMEOUT is still set.  (A launch
+ * captured in a CUDA graph keeps its epoch on every replay: after a replay gave up, clear the word
+ * with pa_device_error_flags(1, ...) before replaying the graph again.)  This call launches one CTA
+ * that does exactly that on barriers nothing completes: warp 0 gives up after limit_ns and records
+ * the timeout, warp 1 (limit 1 s) must leave as soon as it sees it.  Nothing faults and the context
+ * stays usable.
  *   limit_ns     warp 0's limit, 1000 .. 1000000000 (else PA_EINVAL)
  *   elapsed_ns   optional device uint64_t[2]: how long warp 0's and warp 1's waits took
- * Read the outcome with pa_device_error_flags(1, stream), which also clears the bit: while
- * PA_DEVERR_TIMEOUT stays set, later waits that need more than a few tries give up early.
+ * Read the outcome with pa_device_error_flags(clear, stream).
  */
 PA_API int pa_selftest_bounded_wait(int64_t limit_ns, void* elapsed_ns, void* stream);
 

@@ -23,7 +23,6 @@
 //
 // The tile loop inside a warp visits tokens in increasing logical order, so the result depends
 // only on logical positions, not on where the blocks sit in the pool.
-#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -77,9 +76,8 @@ struct TcCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;  // K and V
   static constexpr int kStages = D == 128 ? PA_TC_STAGES_128 : PA_TC_STAGES_64;  // per warp
-  static constexpr int kPartialBytes = (8 * D + 16) * 4;  // one CTA's (acc, max, sum) for up to 8 heads
   static constexpr int kSmemBytes =
-      1024 /*barriers*/ + 1024 /*alignment*/ + kTcWarps * kStages * kStageBytes + kPartialBytes;
+      1024 /*barriers*/ + 1024 /*alignment*/ + kTcWarps * kStages * kStageBytes;
   static_assert(kTcWarps * kStages * 8 <= 1024, "barriers must fit their 1 KB slot");
 };
 
@@ -217,7 +215,7 @@ __device__ __forceinline__ void tile_update(uint8_t* st, int valid, const uint32
   }
 }
 
-template <typename T, int D, int G, bool kCluster>
+template <typename T, int D, int G>
 __global__ void __launch_bounds__(kTcWarps * 32, G > 8 ? 2 : PA_TC_MIN_CTAS)
     decode_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
@@ -227,7 +225,6 @@ __global__ void __launch_bounds__(kTcWarps * 32, G > 8 ? 2 : PA_TC_MIN_CTAS)
   constexpr int kKSteps = D / 16;
   constexpr int kDTiles = D / 8;
   static_assert(G <= 16, "query group must fit the 16 rows of the mma tile");
-  static_assert(!kCluster || G <= 8, "the cluster merge stages at most 8 heads");
   constexpr int kRows = RowHalves<G>::kN;
 
   extern __shared__ uint8_t smem_raw[];
@@ -235,12 +232,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, G > 8 ? 2 : PA_TC_MIN_CTAS)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base);
   uint8_t* stages = base + 1024;
 
-  // grid order: KV heads innermost (CTAs touching one physical block run together), or, for the
-  // cluster merge, partitions innermost (one cluster = the partitions of one (row, KV head))
-  const int kvh = kCluster ? (int)((blockIdx.x / a.max_parts) % a.n_kv_heads) : (int)(blockIdx.x % a.n_kv_heads);
-  const int part = kCluster ? (int)(blockIdx.x % a.max_parts) : (int)((blockIdx.x / a.n_kv_heads) % a.max_parts);
-  const int64_t row = kCluster ? (int64_t)(blockIdx.x / a.max_parts) / a.n_kv_heads
-                               : (int64_t)(blockIdx.x / a.n_kv_heads) / a.max_parts;
+  // grid order: KV heads innermost (CTAs touching one physical block run together)
+  const int kvh = (int)(blockIdx.x % a.n_kv_heads);
+  const int part = (int)((blockIdx.x / a.n_kv_heads) % a.max_parts);
+  const int64_t row = (int64_t)(blockIdx.x / a.n_kv_heads) / a.max_parts;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int g = lane >> 2;   // mma row group: query head g of the group
@@ -283,9 +278,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, G > 8 ? 2 : PA_TC_MIN_CTAS)
     len = len < 0 ? 0 : max_len;
   }
   const int n_parts_row = len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
-  if (!kCluster && part >= n_parts_row) return;
-  const bool active = part < n_parts_row;  // a cluster's surplus CTAs stay for the barriers
-  const int64_t t_end = active ? min(t_begin + a.part_tokens, len) : t_begin;
+  if (part >= n_parts_row) return;
+  const int64_t t_end = min(t_begin + a.part_tokens, len);
   const int n_tiles = (int)((t_end - t_begin + kTile - 1) / kTile);
   const int my_tiles = n_tiles > warp ? (n_tiles - warp + kTcWarps - 1) / kTcWarps : 0;
   const int bmask = a.block_size - 1;
@@ -346,7 +340,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, G > 8 ? 2 : PA_TC_MIN_CTAS)
   int j_fail = my_tiles;  // first tile whose wait gave up
   for (int j = 0; j < my_tiles; ++j) {
     const int s = j % kStages;
-    if (!__all_sync(0xffffffffu, mbar_wait(&my_bars[s], (unsigned)((j / kStages) & 1), a.err))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&my_bars[s], (unsigned)((j / kStages) & 1), a.err, a.epoch))) {
       timed_out = true;
       j_fail = j;
       break;
@@ -373,7 +367,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, G > 8 ? 2 : PA_TC_MIN_CTAS)
     if (lane == 0 && j + kStages < my_tiles) issue(j + kStages, tile_block(j + kStages));
   }
   if (timed_out && lane == 0) {
-    raise_error(a.err, PA_DEVERR_TIMEOUT);
+    raise_timeout(a.err, a.epoch);
     // leave no copy in flight: wait (bounded) for the tiles issued from j_fail on
     const int issued = j_fail + kStages < my_tiles ? j_fail + kStages : my_tiles;
     for (int j = j_fail; j < issued; ++j) mbar_wait(&my_bars[j % kStages], (unsigned)((j / kStages) & 1));
@@ -427,14 +421,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, G > 8 ? 2 : PA_TC_MIN_CTAS)
       }
     }
     const int64_t qh = row * a.n_q_heads + (int64_t)kvh * G + h;
-    if (kCluster) {
-      float* cp = reinterpret_cast<float*>(stages + kTcWarps * kStages * kStageBytes);
-      cp[h * D + d] = A;
-      if (d == 0) {
-        cp[G * D + h] = M;
-        cp[G * D + G + h] = L;
-      }
-    } else if (direct) {
+    if (direct) {
       static_cast<T*>(a.out)[qh * D + d] = Elt<T>::from_float(L != 0.f ? A / L : 0.f);
     } else {
       const int64_t pi = qh * a.max_parts + part;
@@ -445,300 +432,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, G > 8 ? 2 : PA_TC_MIN_CTAS)
       }
     }
   }
-  if constexpr (kCluster) {
-    // log-sum-exp merge of the cluster's partitions through distributed shared memory: rank 0 reads
-    // every rank's (acc, max, sum) once all are written, the others stay resident until it is done
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    if (part == 0) {
-      float* cp = reinterpret_cast<float*>(stages + kTcWarps * kStages * kStageBytes);
-      for (int i = threadIdx.x; i < G * D; i += kTcWarps * 32) {
-        const int h = i / D;
-        const int d = i - h * D;
-        float M = -INFINITY;
-        for (int p = 0; p < a.max_parts; ++p) {
-          const float* rp = cluster.map_shared_rank(cp, p);
-          if (rp[G * D + G + h] != 0.f) M = fmaxf(M, rp[G * D + h]);
-        }
-        float L = 0.f, A = 0.f;
-        if (M != -INFINITY) {
-          for (int p = 0; p < a.max_parts; ++p) {
-            const float* rp = cluster.map_shared_rank(cp, p);
-            const float lp = rp[G * D + G + h];
-            if (lp != 0.f) {
-              const float f = fast_exp2(rp[G * D + h] - M);
-              L = fmaf(lp, f, L);
-              A = fmaf(rp[h * D + d], f, A);
-            }
-          }
-        }
-        const int64_t qh = row * a.n_q_heads + (int64_t)kvh * G + h;
-        static_cast<T*>(a.out)[qh * D + d] = Elt<T>::from_float(L != 0.f ? A / L : 0.f);
-      }
-    }
-    cluster.sync();
-  }
 }
 
-// ------------------------------------------------------------------------------------------------
-// Equal-work grid.  Per KV head, the 16-token tiles of all sequences are laid end to end
-// (sequence 0's tiles, then sequence 1's, ...) and cut into n_units = n_ctas x kTcWarps ranges of
-// `per` consecutive tiles; warp w of CTA (c, kvh) streams range c * kTcWarps + w through its own
-// TMA ring.  per = max(ceil(total / n_units), ceil(t_max / (slots - 1))), t_max the longest
-// sequence's tile count and slots = a.max_parts the split-K slots per row, so that no sequence
-// meets more ranges than it has slots.  The grid is one wave
-// (n_ctas x n_kv_heads CTAs resident at once), so every warp streams the same number of bytes,
-// none waits for another (there is no barrier in the kernel) and none waits for a straggler CTA;
-// the warps of one range index (one per KV head) read the same physical blocks at the same time.
-// A range meets a sequence in one segment.  At each segment end the warp writes the output (a
-// sequence inside one range) or the segment's partial state into the sequence's split-K slot
-// q - q_first(b), where q is the range and q_first(b) the range holding the sequence's first tile;
-// the warp holding that first tile also records the sequence's number of slots for the merge
-// kernel.  A sequence of t tiles meets at most ceil(t / per) + 1 <= slots ranges.
-// ------------------------------------------------------------------------------------------------
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kTcWarps * 32, G > 8 ? 2 : PA_TC_MIN_CTAS)
-    decode_bal_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap vmap) {
-  constexpr int kHalves = TcCfg<D>::kHalves;
-  constexpr int kStageBytes = TcCfg<D>::kStageBytes;
-  constexpr int kStages = TcCfg<D>::kStages;
-  constexpr int kKSteps = D / 16;
-  constexpr int kDTiles = D / 8;
-  static_assert(G <= 16, "query group must fit the 16 rows of the mma tile");
-  constexpr int kRows = RowHalves<G>::kN;
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base);
-  uint8_t* stages = base + 1024;
-
-  const int kvh = (int)(blockIdx.x % a.n_kv_heads);
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int q_unit = (int)(blockIdx.x / a.n_kv_heads) * kTcWarps + warp;  // this warp's range
-  const int n_units = (int)(gridDim.x / a.n_kv_heads) * kTcWarps;
-  const int g = lane >> 2;
-  const int tig = lane & 3;
-  const int64_t max_len = a.bt_stride << a.block_shift;
-  const int bmask = a.block_size - 1;
-
-  auto len_of = [&](int b) -> int64_t {
-    const int64_t n = __ldg(a.context_lens + b);
-    return n < 0 ? 0 : (n > max_len ? max_len : n);
-  };
-  auto tiles_of = [&](int b) -> int64_t { return (len_of(b) + kTile - 1) / kTile; };
-
-  pdl_wait_primary();       // the preceding grid has completed (see decode_tc_kernel)
-  pdl_launch_dependents();  // the split-K merge may begin launching; it waits for this grid's results
-
-  // ---- this warp's range [r0, r1) of the concatenated tiles --------------------------------------
-  int64_t total = 0, t_max = 0;
-  for (int b0 = 0; b0 < a.batch; b0 += 32) {
-    const int b = b0 + lane;
-    int64_t t = 0;
-    if (b < a.batch) {
-      const int64_t n = __ldg(a.context_lens + b);
-      if ((n < 0 || n > max_len) && blockIdx.x == 0 && warp == 0) raise_error(a.err, PA_DEVERR_CONTEXT_LEN);
-      t = tiles_of(b);
-    }
-    int64_t tm = t;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      t += __shfl_xor_sync(0xffffffffu, t, off);
-      tm = max(tm, __shfl_xor_sync(0xffffffffu, tm, off));
-    }
-    total += t;
-    t_max = max(t_max, tm);
-  }
-  const int64_t per_slots = (t_max + a.max_parts - 2) / (a.max_parts - 1);  // ceil(t_max / (slots - 1))
-  const int64_t per = max(max((total + n_units - 1) / n_units, per_slots), (int64_t)1);
-  const int64_t r0 = (int64_t)q_unit * per;
-  if (r0 >= total) return;  // nothing left for this range (no barrier follows in this kernel)
-  const int64_t r1 = min(r0 + per, total);
-  const int my_tiles = (int)(r1 - r0);
-  // first sequence with a tile in the range: the smallest b with o_b + t_b > r0
-  int b_first = 0;
-  int64_t o_first = 0;
-  {
-    int64_t run = 0;
-    for (int b0 = 0; b0 < a.batch; b0 += 32) {
-      const int b = b0 + lane;
-      const int64_t t = b < a.batch ? tiles_of(b) : 0;
-      int64_t incl = t;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      const unsigned hit = __ballot_sync(0xffffffffu, b < a.batch && run + incl > r0);
-      if (hit != 0u) {
-        const int l = __ffs(hit) - 1;
-        b_first = b0 + l;
-        o_first = run + __shfl_sync(0xffffffffu, incl - t, l);
-        break;
-      }
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
-
-  uint64_t* my_bars = bars + warp * kStages;
-  uint8_t* my_stages = stages + warp * kStages * kStageBytes;
-  if (lane == 0) {
-    prefetch_tensormap(&kmap);
-    prefetch_tensormap(&vmap);
-    for (int s = 0; s < kStages; ++s) mbar_init(&my_bars[s], 1);
-    fence_barrier_init();
-    fence_proxy_async_smem();
-  }
-  __syncwarp();
-
-  // producer cursor (lane 0): sequence pb holds the next tile to issue; its tiles start at pob
-  int pb = b_first;
-  int64_t pob = o_first, pnt = tiles_of(b_first);
-  int issued = 0;
-  const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once per launch
-  auto issue = [&](int k) {  // lane 0 only: the range's k-th tile
-    const int64_t u = r0 + k;
-    while (pob + pnt <= u) {
-      pob += pnt;
-      ++pb;
-      pnt = tiles_of(pb);
-    }
-    const int64_t t0 = (u - pob) * kTile;
-    const int blk = __ldg(a.block_table + (int64_t)pb * a.bt_stride + (t0 >> a.block_shift));
-    const int s = k % kStages;
-    ++issued;
-    if (blk < 0 || blk >= a.num_blocks) {
-      raise_error(a.err, PA_DEVERR_BLOCK_ID);
-      mbar_arrive(&my_bars[s]);  // complete the phase without data; the consumer skips the tile
-      return;
-    }
-    const int off = (int)(t0 & bmask);
-    uint8_t* st = my_stages + s * kStageBytes;
-    mbar_arrive_expect_tx(&my_bars[s], kStageBytes);
-#pragma unroll
-    for (int h = 0; h < kHalves; ++h)
-      load_kv_box(st + h * kHalfBytes, &kmap, kvh * D + h * 64, off, blk, &my_bars[s], kv_policy);
-#pragma unroll
-    for (int h = 0; h < kHalves; ++h)
-      load_kv_box(st + (kHalves + h) * kHalfBytes, &vmap, kvh * D + h * 64, off, blk, &my_bars[s], kv_policy);
-  };
-  if (lane == 0) {
-    const int pre = my_tiles < kStages ? my_tiles : kStages;
-    for (int k = 0; k < pre; ++k) issue(k);
-  }
-
-  int k = 0;        // tiles consumed
-  int k_fail = -1;  // first tile whose wait gave up
-  int b = b_first;
-  int64_t ob = o_first;
-  while (ob < r1) {
-    const int64_t len = len_of(b);
-    const int64_t nt = (len + kTile - 1) / kTile;
-    if (nt == 0) {  // an empty sequence has no tile in any range (the merge kernel writes its zeros)
-      ++b;
-      continue;
-    }
-    const int64_t g0 = max(ob, r0), g1 = min(ob + nt, r1);
-    const int32_t* table = a.block_table + (int64_t)b * a.bt_stride;
-    // fused write: the range holding the sequence's last tile writes this step's K/V row
-    int64_t new_row = -1;
-    if (a.k_new != nullptr && g1 == ob + nt) {
-      const int64_t last = len - 1;
-      const int64_t s_new = __ldg(a.slot_mapping + b);
-      const int blk_last = __ldg(table + (last >> a.block_shift));
-      const int64_t expect = (blk_last >= 0 && blk_last < a.num_blocks)
-                                 ? ((int64_t)blk_last << a.block_shift) + (last & bmask) : -2;
-      if (s_new >= 0) {
-        if (s_new == expect)
-          new_row = (int64_t)blk_last * a.kv_block_stride + (last & bmask) * ((int64_t)a.n_kv_heads * D);
-        else if (lane == 0)
-          raise_error(a.err, PA_DEVERR_SLOT);
-      }
-    }
-    uint32_t qa[kKSteps][4];
-    load_q_frags<T, D, G>(a, b, kvh, lane, qa);
-    float o[kDTiles][4];
-#pragma unroll
-    for (int i = 0; i < kDTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    bool have = false;
-    for (int64_t u = g0; u < g1; ++u, ++k) {
-      if (k_fail >= 0) continue;
-      const int s = k % kStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(&my_bars[s], (unsigned)((k / kStages) & 1), a.err))) {
-        k_fail = k;
-        continue;
-      }
-      const int64_t t0 = (u - ob) * kTile;
-      const int blk = __ldg(table + (t0 >> a.block_shift));
-      const int valid = (int)(len - t0 < kTile ? len - t0 : kTile);
-      uint8_t* st = my_stages + s * kStageBytes;
-      if (blk >= 0 && blk < a.num_blocks) {
-        if (new_row >= 0 && u == ob + nt - 1) {
-          const int64_t src_off = ((int64_t)b * a.n_kv_heads + kvh) * D;
-          const int64_t dst_off = new_row + (int64_t)kvh * D;
-          patch_new_token<T, D>(st, (int)((len - 1) & (kTile - 1)), static_cast<const T*>(a.k_new) + src_off,
-                                static_cast<const T*>(a.v_new) + src_off, static_cast<T*>(a.k_pool_w) + dst_off,
-                                static_cast<T*>(a.v_pool_w) + dst_off, lane);
-        }
-        tile_update<T, D, G>(st, valid, qa, o, m_run, l_run, a.scale_log2, lane);
-        have = true;
-      }
-      // release the stage and refill it with the range's tile k + kStages
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0 && k + kStages < my_tiles) issue(k + kStages);
-    }
-    // ---- segment end: output or partial state of the rows holding query heads ---------------------
-    const bool whole = g0 == ob && g1 == ob + nt;
-    const int64_t q_first = ob / per;
-#pragma unroll
-    for (int hh = 0; hh < kRows; ++hh) {
-      float lr = l_run[hh];
-      lr += __shfl_xor_sync(0xffffffffu, lr, 1);
-      lr += __shfl_xor_sync(0xffffffffu, lr, 2);
-      const float l_out = have && k_fail < 0 ? lr : 0.f;
-      const int gr = g + 8 * hh;  // query head of this row
-      if (gr < G) {
-        const int64_t qh = (int64_t)b * a.n_q_heads + (int64_t)kvh * G + gr;
-        if (whole) {
-          const float inv = l_out != 0.f ? 1.f / l_out : 0.f;
-          T* orow = static_cast<T*>(a.out) + qh * D;
-#pragma unroll
-          for (int i = 0; i < kDTiles; ++i) {
-            T* dst = orow + i * 8 + 2 * tig;
-            dst[0] = Elt<T>::from_float(o[i][2 * hh] * inv);
-            dst[1] = Elt<T>::from_float(o[i][2 * hh + 1] * inv);
-          }
-        } else {
-          const int64_t pi = qh * a.max_parts + (q_unit - q_first);
-          float* acc = a.ws_acc + pi * D;
-#pragma unroll
-          for (int i = 0; i < kDTiles; ++i)
-            *reinterpret_cast<float2*>(acc + i * 8 + 2 * tig) = make_float2(o[i][2 * hh], o[i][2 * hh + 1]);
-          if (tig == 0) {
-            a.ws_m[pi] = m_run[hh];
-            a.ws_l[pi] = l_out;
-          }
-        }
-      }
-    }
-    if (kvh == 0 && g0 == ob && lane == 0) a.ws_np[b] = whole ? 1 : (int)((ob + nt - 1) / per - q_first + 1);
-    ob += nt;
-    ++b;
-  }
-  if (k_fail >= 0 && lane == 0) {
-    raise_error(a.err, PA_DEVERR_TIMEOUT);
-    // leave no copy in flight: wait (bounded) for the tiles issued from k_fail on
-    for (int j = k_fail; j < issued; ++j) mbar_wait(&my_bars[j % kStages], (unsigned)((j / kStages) & 1));
-  }
-}
-
-// ------------------------------------------------------------------------------------------------
-// host side: tensor maps and dispatch
 // ------------------------------------------------------------------------------------------------
 namespace {
 
@@ -810,7 +505,7 @@ bool decode_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, i
   return encode_fn() != nullptr;
 }
 
-template <typename T, int D, int G, bool kCluster>
+template <typename T, int D, int G>
 static cudaError_t launch_tc_g(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
   constexpr int smem = TcCfg<D>::kSmemBytes;
   static bool attr_set[64] = {};  // per instantiation and device; idempotent, so a race is harmless
@@ -818,7 +513,7 @@ static cudaError_t launch_tc_g(const AttnArgs& a, const CUtensorMap& km, const C
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_tc_kernel<T, D, G, kCluster>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(decode_tc_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
@@ -830,36 +525,24 @@ static cudaError_t launch_tc_g(const AttnArgs& a, const CUtensorMap& km, const C
   cfg.blockDim = dim3(kTcWarps * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
+  // programmatic dependent launch: the grid may start while the preceding kernel of the stream
+  // (typically the previous step's merge) finishes; the kernel waits for it before any global access
   cudaLaunchAttribute attr[1];
-  if (kCluster) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)a.max_parts;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-  } else {
-    // programmatic dependent launch: the grid may start while the preceding kernel of the stream
-    // (typically the previous step's merge) finishes; the kernel waits for it before any global access
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-  }
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = kCluster || PA_DECODE_PDL ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, D, G, kCluster>, a, km, vm);
-}
-
-template <typename T, int D, int G>
-static cudaError_t launch_tc_c(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
-  return a.cluster ? launch_tc_g<T, D, G, true>(a, km, vm, s) : launch_tc_g<T, D, G, false>(a, km, vm, s);
+  cfg.numAttrs = PA_DECODE_PDL ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, D, G>, a, km, vm);
 }
 
 template <typename T, int D>
 static cudaError_t launch_tc_d(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
   switch (a.group) {
-    case 1: return launch_tc_c<T, D, 1>(a, km, vm, s);
-    case 2: return launch_tc_c<T, D, 2>(a, km, vm, s);
-    case 4: return launch_tc_c<T, D, 4>(a, km, vm, s);
-    case 8: return launch_tc_c<T, D, 8>(a, km, vm, s);
-    case 16: return launch_tc_g<T, D, 16, false>(a, km, vm, s);  // no cluster merge for 16 heads
+    case 1: return launch_tc_g<T, D, 1>(a, km, vm, s);
+    case 2: return launch_tc_g<T, D, 2>(a, km, vm, s);
+    case 4: return launch_tc_g<T, D, 4>(a, km, vm, s);
+    case 8: return launch_tc_g<T, D, 8>(a, km, vm, s);
+    case 16: return launch_tc_g<T, D, 16>(a, km, vm, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -876,76 +559,6 @@ cudaError_t launch_decode_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int
       !encode_pool_map(&vm, a.v_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride))
     return cudaErrorInvalidValue;
   cudaError_t e = dt == PA_BF16 ? launch_tc_t<__nv_bfloat16>(a, km, vm, s) : launch_tc_t<__half>(a, km, vm, s);
-  ++*launches;
-  return e;
-}
-
-template <typename T, int D, int G>
-static cudaError_t launch_bal_g(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
-  constexpr int smem = 1024 /*barriers*/ + 1024 /*alignment*/ + kTcWarps * TcCfg<D>::kStages * TcCfg<D>::kStageBytes;
-  static int ctas_per_sm[64] = {};  // per instantiation and device: resident CTAs per SM at this smem
-  static int sm_count[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  int per_sm = dev >= 0 && dev < 64 ? ctas_per_sm[dev] : 0;
-  int sms = dev >= 0 && dev < 64 ? sm_count[dev] : 0;
-  if (per_sm == 0 || sms == 0) {
-    e = cudaFuncSetAttribute(decode_bal_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_bal_kernel<T, D, G>, kTcWarps * 32, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    if (dev >= 0 && dev < 64) {
-      ctas_per_sm[dev] = per_sm;
-      sm_count[dev] = sms;
-    }
-  }
-  // one wave: n_ctas ranges per KV head, n_ctas x n_kv_heads CTAs resident together
-  int64_t n_ctas = (int64_t)per_sm * sms / a.n_kv_heads;
-  if (n_ctas < 1) n_ctas = 1;
-  const int64_t grid = n_ctas * a.n_kv_heads;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kTcWarps * 32);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // as in launch_tc_g
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = PA_DECODE_PDL ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_bal_kernel<T, D, G>, a, km, vm);
-}
-
-template <typename T, int D>
-static cudaError_t launch_bal_d(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
-  switch (a.group) {
-    case 1: return launch_bal_g<T, D, 1>(a, km, vm, s);
-    case 2: return launch_bal_g<T, D, 2>(a, km, vm, s);
-    case 4: return launch_bal_g<T, D, 4>(a, km, vm, s);
-    case 8: return launch_bal_g<T, D, 8>(a, km, vm, s);
-    case 16: return launch_bal_g<T, D, 16>(a, km, vm, s);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-template <typename T>
-static cudaError_t launch_bal_t(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t s) {
-  return a.head_dim == 64 ? launch_bal_d<T, 64>(a, km, vm, s) : launch_bal_d<T, 128>(a, km, vm, s);
-}
-
-cudaError_t launch_decode_bal(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches) {
-  if (a.rows == 0) return cudaSuccess;
-  if (a.ws_np == nullptr || a.ws_acc == nullptr || a.max_parts < 2) return cudaErrorInvalidValue;
-  CUtensorMap km, vm;
-  if (!encode_pool_map(&km, a.k_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride) ||
-      !encode_pool_map(&vm, a.v_pool, dt, a.num_blocks, a.block_size, a.n_kv_heads, a.head_dim, a.kv_block_stride))
-    return cudaErrorInvalidValue;
-  cudaError_t e = dt == PA_BF16 ? launch_bal_t<__nv_bfloat16>(a, km, vm, s) : launch_bal_t<__half>(a, km, vm, s);
   ++*launches;
   return e;
 }

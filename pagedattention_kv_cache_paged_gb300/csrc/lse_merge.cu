@@ -36,11 +36,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
   const float* pl = a.part_l + row * a.n_parts;
   const float* pacc = a.part_acc + row * a.n_parts * (int64_t)D + lane * kPer;
   // Every load that does not depend on the partition count goes out at once (one round trip to
-  // memory instead of three): the row's length and slot count, (max, sum) of partition `lane`, and
-  // this lane's head_dim slice of the first kSpec partitions' accumulators.
+  // memory instead of three): the row's length, (max, sum) of partition `lane`, and this lane's
+  // head_dim slice of the first kSpec partitions' accumulators.
   const int64_t seq = a.context_lens != nullptr ? row / a.heads_per_seq : 0;
   int64_t len = a.context_lens != nullptr ? __ldg(a.context_lens + seq) : 0;
-  const int sp = a.seq_parts != nullptr ? __ldg(a.seq_parts + seq) : 0;
   const float m_l = lane < a.n_parts ? pm[lane] : -INFINITY;
   const float l_l = lane < a.n_parts ? pl[lane] : 0.f;
   float accs[kSpec][kPer];
@@ -52,18 +51,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
   int parts = a.n_parts;
   if (a.context_lens != nullptr) {
     len = len < 0 ? 0 : (len > a.max_len ? a.max_len : len);
-    if (a.seq_parts != nullptr) {
-      // equal-work grid: an empty sequence met no range; the others say how many slots they use
-      if (len == 0) {
-        T* o = static_cast<T*>(a.out) + row * D + lane * kPer;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) o[i] = Elt<T>::from_float(0.f);
-        return;
-      }
-      parts = sp > a.n_parts ? a.n_parts : sp;
-    } else {
-      parts = len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
-    }
+    parts = len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
     if (parts <= 1) return;  // written directly by the partition kernel
   }
   // the row maximum over partitions that hold tokens: lane p looks at partitions p, p + 32, ...
@@ -121,23 +109,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Merge
 constexpr int kWideParts = 16;
 constexpr int kWideWarps = 8;
 
-// Number of partitions of row `row` that hold partial states (0: the row is empty and was written
-// here as zeros; 1: written directly by the partition kernel); shared by both merge kernels.
-template <typename T, int D>
-__device__ __forceinline__ int merge_parts(const MergeArgs& a, int64_t row, int tid, int nthreads) {
+// Number of partitions of row `row` that hold partial states (1: the row was written directly by
+// the partition kernel).
+__device__ __forceinline__ int merge_parts(const MergeArgs& a, int64_t row) {
   if (a.context_lens == nullptr) return a.n_parts;
   const int64_t seq = row / a.heads_per_seq;
   int64_t len = __ldg(a.context_lens + seq);
   len = len < 0 ? 0 : (len > a.max_len ? a.max_len : len);
-  if (a.seq_parts != nullptr) {
-    if (len == 0) {
-      T* o = static_cast<T*>(a.out) + row * D;
-      for (int i = tid; i < D; i += nthreads) o[i] = Elt<T>::from_float(0.f);
-      return 0;
-    }
-    const int sp = __ldg(a.seq_parts + seq);
-    return sp > a.n_parts ? a.n_parts : sp;
-  }
   return len == 0 ? 1 : (int)((len + a.part_tokens - 1) / a.part_tokens);
 }
 
@@ -151,7 +129,7 @@ __global__ void __launch_bounds__(kWideWarps * 32) lse_merge_wide_kernel(const M
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();  // the next step's decode grid may begin launching (it waits for this grid)
   pdl_wait_primary();       // partials of the partition kernel are complete and visible
-  const int parts = merge_parts<T, D>(a, row, threadIdx.x, kWideWarps * 32);  // uniform over the CTA
+  const int parts = merge_parts(a, row);  // uniform over the CTA
   if (parts <= 1) return;
   const float* pm = a.part_m + row * a.n_parts;
   const float* pl = a.part_l + row * a.n_parts;

@@ -13,6 +13,12 @@ namespace pa {
 // Element size of an I/O dtype in bytes.
 inline int dtype_bytes(pa_dtype dt) { return dt == PA_FP32 ? 4 : 2; }
 
+// Record a CUDA error for pa_last_cuda_error() on this thread and return PA_ECUDA.
+int fail_cuda(cudaError_t e);
+
+// The calling thread's current CUDA context (identifies a device's context across resets).
+int current_context(void** ctx);
+
 struct KvWriteArgs {
   const void* k_new;
   const void* v_new;
@@ -81,10 +87,8 @@ struct AttnArgs {
   float* ws_m;                     // [rows * n_q_heads][max_parts]
   float* ws_l;                     // [rows * n_q_heads][max_parts]
   float* ws_acc;                   // [rows * n_q_heads][max_parts][head_dim]
-  // equal-work decode grid only (nullptr otherwise): per sequence, the number of split-K slots its
-  // partial states occupy (1 = written directly); max_parts is then the slot stride per row
-  int32_t* ws_np;
-  unsigned* err;
+  unsigned* err;                   // device error word pair ([0] bits, [1] epoch of a launch that gave up)
+  unsigned epoch;                  // this launch's epoch (never 0): its bounded waits abort only on it
   // fused K/V write (decode only; all nullptr otherwise): sequence b's new token k_new[b], v_new[b]
   // ([batch][n_kv_heads][head_dim]) goes to pool row slot_mapping[b], which must be the slot of its
   // last context position; the CTA reading that position takes the row from k_new/v_new directly.
@@ -93,9 +97,6 @@ struct AttnArgs {
   const int64_t* slot_mapping;
   void* k_pool_w;                  // the pools again, writable
   void* v_pool_w;
-  // tensor-core decode: 1 = the partitions of a row form one thread-block cluster and merge their
-  // partial states through distributed shared memory (no workspace, no merge kernel)
-  int cluster;
 };
 
 struct MergeArgs {
@@ -113,9 +114,6 @@ struct MergeArgs {
   int heads_per_seq;
   int part_tokens;
   int64_t max_len;                 // clamp for context_lens (bt_stride * block_size)
-  // equal-work decode grid: when seq_parts != nullptr (with context_lens), sequence s's rows hold
-  // seq_parts[s] partials (<= n_parts; 1 = written directly) and empty sequences are written as zeros
-  const int32_t* seq_parts;
 };
 
 // Launchers: return cudaSuccess or the launch error.  `launches` is incremented per kernel.
@@ -138,19 +136,13 @@ bool encode_q_map(CUtensorMap* map, const void* q, pa_dtype dt, int64_t total_q,
 // Tensor-core decode (TMA + mma.sync) for bf16/fp16 pools with block_size % 16 == 0.
 bool decode_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks);
 cudaError_t launch_decode_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
-// Equal-work split-K grid of the same kernel math (needs a.ws_np and the workspace; a.max_parts is
-// the slot stride per row, at least 2).
-cudaError_t launch_decode_bal(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
 
-// Tensor-core causal prefill (TMA ring + mma.sync) for bf16/fp16 pools with block_size % 16 == 0.
-bool prefill_tc_supported(pa_dtype dt, int block_size, int head_dim, int group, int64_t num_blocks);
-cudaError_t launch_prefill_tc(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
-
-// tcgen05 causal prefill (TMEM accumulators, TMA ring, warp-specialised), same support set.
+// tcgen05 causal prefill (TMEM accumulators, TMA rings, warp-specialised) for bf16/fp16 pools with
+// block_size % 16 == 0 (the support set of the tensor-core decode).
 cudaError_t launch_prefill_umma(const AttnArgs& a, pa_dtype dt, cudaStream_t s, int* launches);
 
 // Bounded-wait self-test (selftest.cu): one CTA whose two waits run out; see pa_selftest_bounded_wait.
-cudaError_t launch_selftest_wait(unsigned* err, uint64_t limit_ns, unsigned long long* elapsed_ns, cudaStream_t s,
-                                 int* launches);
+cudaError_t launch_selftest_wait(unsigned* err, unsigned epoch, uint64_t limit_ns, unsigned long long* elapsed_ns,
+                                 cudaStream_t s, int* launches);
 
 }  // namespace pa

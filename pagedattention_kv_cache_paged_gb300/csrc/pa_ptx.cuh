@@ -78,9 +78,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Between tries the wait also
-// watches `abort_word` (the device error word): once any CTA has recorded a timeout, the others stop
-// waiting too, so a broken launch ends after about one timeout period instead of one per CTA.
-__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, unsigned parity, const unsigned* abort_word,
+// watches the launch's abort slot: err[1] of the device error word pair holds the epoch of the last
+// launch whose wait gave up (raise_timeout), so once any warp or CTA of this launch has given up
+// the others stop waiting too and a broken launch ends after about one timeout period instead of
+// one per CTA.  Another launch's epoch there does not stop this one.  err == nullptr: no abort.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, unsigned parity, const unsigned* err, unsigned epoch,
                                               uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -88,16 +90,23 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, unsigned parity, co
     if (kWaitSleepNs) __nanosleep(kWaitSleepNs);
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 15u) == 0) {
-      if (abort_word != nullptr &&
-          (*reinterpret_cast<const volatile unsigned*>(abort_word) & 32u /* PA_DEVERR_TIMEOUT */))
-        return false;
+      if (err != nullptr && *reinterpret_cast<const volatile unsigned*>(err + 1) == epoch) return false;
       if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }
 }
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, const unsigned* abort_word = nullptr) {
-  return mbar_wait_for(bar, parity, abort_word, kWaitLimitNs);
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, const unsigned* err = nullptr,
+                                          unsigned epoch = 0) {
+  return mbar_wait_for(bar, parity, err, epoch, kWaitLimitNs);
+}
+
+// A bounded wait of this launch gave up: record PA_DEVERR_TIMEOUT and publish the launch's epoch so
+// that its other waits leave too.
+__device__ __forceinline__ void raise_timeout(unsigned* err, unsigned epoch) {
+  if (err == nullptr) return;
+  atomicOr(err, 32u /* PA_DEVERR_TIMEOUT */);
+  atomicExch(err + 1, epoch);
 }
 
 // 2-D tiled TMA load global -> shared, completing `bytes` on `bar`.  x is the inner coordinate.

@@ -1,9 +1,9 @@
 // tcgen05 causal chunked prefill over a paged history (bf16/fp16, block_size % 16 == 0).
 //
-// Computes the same thing as prefill_tc.cu — JuliaPagedAttn README "Features" (batched prefill)
-// with the online softmax of "Online Softmax": the chunk of m_b queries holds the last m_b
-// positions of sequence b's context and query r attends to positions 0 .. n_b - m_b + r through
-// the block table — on the 5th-generation tensor cores with accumulators in tensor memory.
+// JuliaPagedAttn README "Features" (batched prefill) with the online softmax of "Online Softmax":
+// the chunk of m_b queries holds the last m_b positions of sequence b's context and query r
+// attends to positions 0 .. n_b - m_b + r through the block table.  Computed on the 5th-generation
+// tensor cores with accumulators in tensor memory.
 //
 // Persistent: one CTA per SM walks the work items (blockIdx, blockIdx + gridDim, ...).  An item =
 // 256 (query token, head) rows of one KV head, split into two 128-row Q tiles that share every K/V
@@ -24,10 +24,11 @@
 //              O_k += P_k V (M 128, N head_dim, P read from TMEM, V an MN-major shared-memory
 //              operand) with tcgen05.mma in the order S_0(j), P_1(j-1) V, S_1(j), P_0(j) V, so
 //              that the tensor core works on one group's products while the other group computes
-//              its softmax.  S_k of the next tile is issued only after O_k += P_k V of this one has
-//              completed, because P_k lives in the columns the next S_k overwrites; that same
-//              ordering makes O_k stable whenever a group sees a new S_k, so rescaling needs no
-//              extra wait.
+//              its softmax.  P_k lives in the columns the next S_k overwrites: S_k of the next
+//              tile is issued right after O_k += P_k V of this one, and tcgen05 products of one
+//              thread run in issue order, so the P V reads P_k first.  The commit that signals
+//              the new S_k also covers that P V, so O_k is stable whenever a group sees a new S_k
+//              and rescaling needs no extra wait.
 // Every mbarrier wait is bounded (PA_DEVERR_TIMEOUT, with a cooperative abort); TMEM is always
 // released.  The stabilising maximum is exact bookkeeping: numerator and denominator use the
 // same one, so the result equals the running-max form of "Online Softmax" in real arithmetic.
@@ -63,6 +64,13 @@ constexpr float kUmRescaleThreshold = 8.f;  // log2 units: O is rescaled when th
 #define PA_UM_PERSISTENT 1
 #endif
 constexpr bool kUmPersistent = PA_UM_PERSISTENT != 0;
+// 0: S_k of the next tile is issued right after O_k += P_k V of this tile (tcgen05.mma products of
+// one thread run in issue order, so the P V reads P_k before the next S_k overwrites its columns);
+// 1: only once that P V has completed (measured 4 % slower)
+#ifndef PA_UM_S_AFTER_PV_DONE
+#define PA_UM_S_AFTER_PV_DONE 0
+#endif
+constexpr bool kUmSAfterPvDone = PA_UM_S_AFTER_PV_DONE != 0;
 
 template <int D>
 struct UmCfg {
@@ -83,41 +91,6 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c, int half_bytes) {
 // Softmax helpers: one thread owns one row of S (its TMEM lane); `taddr` is the row's first column.
 // Keys whose bit is clear in mask[q] (chunk q = columns 32q .. 32q + 31) are outside the causal
 // bound or were not loaded; kMasked = false is the common case of a tile with every key valid.
-
-// Pairs out of every 8 whose exponentials run on the FMA pipe (exp2_fma) instead of the MUFU unit,
-// in unmasked tiles: at full tensor rate the MUFU alone would need as many cycles per tile as the
-// tensor core, so moving a share of the exponentials to the FMA pipe leaves it slack.
-#ifndef PA_UM_POLY_PAIRS
-#define PA_UM_POLY_PAIRS 0
-#endif
-constexpr int kUmPolyPairs = PA_UM_POLY_PAIRS;
-static_assert(kUmPolyPairs >= 0 && kUmPolyPairs <= 8, "pairs out of 8");
-
-// 2^x for a pair of arguments on the FMA pipe: Cody-Waite reduction x = n + f with n = round(x),
-// f in [-1/2, 1/2], then a degree-3 polynomial for 2^f (coefficients fitted to minimise the
-// relative error on [-1/2, 1/2]: at most 7.5e-5 in fp32, below half an ulp of bf16 and fp16) scaled
-// by 2^n built in the exponent field.  x is clamped below at -126 (2^-126 instead of a smaller
-// value: invisible next to a row sum of at least 1); a NaN argument gives NaN.
-__device__ __forceinline__ uint64_t exp2_fma2(float x0, float x1) {
-  constexpr float kRound = 12582912.f;  // 1.5 * 2^23: x + kRound holds round(x) in its low mantissa bits
-  constexpr float kC0 = 0.9999280571937561f, kC1 = 0.6932609677314758f, kC2 = 0.2426111251115799f,
-                  kC3 = 0.0551716648042202f;
-  float c0, c1;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(c0) : "f"(x0), "f"(-126.f));
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(c1) : "f"(x1), "f"(-126.f));
-  const uint64_t xc = f2_pack(c0, c1);
-  const uint64_t t = f2_add(xc, f2_pack(kRound, kRound));
-  const uint64_t f = f2_fma(f2_add(t, f2_pack(-kRound, -kRound)), f2_pack(-1.f, -1.f), xc);
-  uint64_t p = f2_fma(f2_pack(kC3, kC3), f, f2_pack(kC2, kC2));
-  p = f2_fma(p, f, f2_pack(kC1, kC1));
-  p = f2_fma(p, f, f2_pack(kC0, kC0));
-  float t0, t1;
-  f2_unpack(t, t0, t1);
-  // (bits of t) * 2^23 keeps n << 23 modulo 2^32; adding the bias gives the bits of 2^n
-  const uint32_t n0 = __float_as_uint(t0) * (1u << 23) + (127u << 23);
-  const uint32_t n1 = __float_as_uint(t1) * (1u << 23) + (127u << 23);
-  return f2_mul(p, f2_pack(__uint_as_float(n0), __uint_as_float(n1)));
-}
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -177,11 +150,7 @@ __device__ __forceinline__ float p_store(uint32_t taddr, const uint32_t (&sv)[N]
         const int j = 64 * h + 2 * c;
         float x0, x1;
         f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])), sc2, nm2), x0, x1);
-        uint64_t e2;
-        if ((c & 7) < kUmPolyPairs)
-          e2 = exp2_fma2(x0, x1);
-        else
-          e2 = f2_pack(fast_exp2(x0), fast_exp2(x1));
+        const uint64_t e2 = f2_pack(fast_exp2(x0), fast_exp2(x1));
         acc2[c & 1] = f2_add(acc2[c & 1], e2);
         float e0, e1;
         f2_unpack(e2, e0, e1);
@@ -404,7 +373,7 @@ __global__ void __launch_bounds__(kUmThreads)
         // both Q tiles of the item, once every S product of the previous item has completed
         bool ok = true;
         if (lane == 0) {
-          ok = nq == 0 || mbar_wait(q_empty, (unsigned)((nq - 1) & 1), a.err);
+          ok = nq == 0 || mbar_wait(q_empty, (unsigned)((nq - 1) & 1), a.err, a.epoch);
           if (ok) {
             mbar_arrive_expect_tx(q_ready, 2 * Cfg::kQBytes);
 #pragma unroll
@@ -416,7 +385,7 @@ __global__ void __launch_bounds__(kUmThreads)
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+          if (lane == 0) raise_timeout(a.err, a.epoch);
           alive = false;
           break;
         }
@@ -431,7 +400,7 @@ __global__ void __launch_bounds__(kUmThreads)
           if (lane == 0) {
             const int s = i % depth;
             const int round = i / depth;
-            ok = round == 0 || mbar_wait(&empty[s], (unsigned)((round - 1) & 1), a.err);
+            ok = round == 0 || mbar_wait(&empty[s], (unsigned)((round - 1) & 1), a.err, a.epoch);
             if (ok) {
               int ys[kUmSub], yo[kUmSub];
               unsigned m = 0;
@@ -475,7 +444,7 @@ __global__ void __launch_bounds__(kUmThreads)
             }
           }
           if (!__shfl_sync(0xffffffffu, ok, 0)) {
-            if (lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+            if (lane == 0) raise_timeout(a.err, a.epoch);
             alive = false;
             break;
           }
@@ -529,7 +498,7 @@ __global__ void __launch_bounds__(kUmThreads)
       bool ok = true;
       if (lane == 0) {
         auto wait = [&](uint64_t* bar, unsigned parity) {
-          ok = ok && mbar_wait(bar, parity, a.err);
+          ok = ok && mbar_wait(bar, parity, a.err, a.epoch);
           return ok;
         };
         // the item's first P V into O_k waits until group k has read O_k of the previous item
@@ -559,11 +528,11 @@ __global__ void __launch_bounds__(kUmThreads)
         for (int j = 0; j < n_all && ok; ++j) {
           const int gj = g + j;
           if (!wait(&kfull[gj % kUmKStages], (unsigned)((gj / kUmKStages) & 1))) break;
-          if (gj > 0 && !wait(&pv_done[0], (unsigned)((gj - 1) & 1))) break;
+          if (kUmSAfterPvDone && gj > 0 && !wait(&pv_done[0], (unsigned)((gj - 1) & 1))) break;
           tc_fence_after();
           issue_s(0, gj);
           if (j > 0 && !pv_of(1, j - 1)) break;
-          if (gj > 0 && !wait(&pv_done[1], (unsigned)((gj - 1) & 1))) break;
+          if (kUmSAfterPvDone && gj > 0 && !wait(&pv_done[1], (unsigned)((gj - 1) & 1))) break;
           tc_fence_after();
           issue_s(1, gj);
           umma_commit(&kempty[gj % kUmKStages]);
@@ -579,10 +548,10 @@ __global__ void __launch_bounds__(kUmThreads)
       g += n_all;
     }
     if (lane == 0) {
-      if (!alive) raise_error(a.err, PA_DEVERR_TIMEOUT);
+      if (!alive) raise_timeout(a.err, a.epoch);
       if (g > 0) {
         umma_commit(fin);
-        mbar_wait(fin, 0, a.err);
+        mbar_wait(fin, 0, a.err, a.epoch);
       }
     }
   } else {
@@ -609,13 +578,13 @@ __global__ void __launch_bounds__(kUmThreads)
         const int nt = tiles_of(sg);
         for (int tile = 0; tile < nt; ++tile, ++i) {
           const int kb = tile * kUmKeys;
-          if (!__all_sync(0xffffffffu, mbar_wait(&mready[i & 7], (unsigned)((i >> 3) & 1), a.err))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&mready[i & 7], (unsigned)((i >> 3) & 1), a.err, a.epoch))) {
             alive = false;
             break;
           }
           const unsigned loaded = kmask[i & 7];
           // S_k of this tile is complete, and with it O_k += P_k V of the previous tile (issued before)
-          if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], (unsigned)(i & 1), a.err))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], (unsigned)(i & 1), a.err, a.epoch))) {
             alive = false;
             break;
           }
@@ -656,7 +625,7 @@ __global__ void __launch_bounds__(kUmThreads)
           // group 0 zeroes V rows that hold no data or lie past the context (group 1's P V is issued
           // after group 0's, so it sees the zeros too)
           if (grp == 0 && (kb + kUmKeys > sg.n || loaded != all_sub)) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&vfull[i % kUmVStages], (unsigned)((i / kUmVStages) & 1), a.err))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&vfull[i % kUmVStages], (unsigned)((i / kUmVStages) & 1), a.err, a.epoch))) {
               alive = false;
               break;
             }
@@ -675,9 +644,9 @@ __global__ void __launch_bounds__(kUmThreads)
         }
         t = sg.seg1;
       }
-      if (!alive && lane == 0) raise_error(a.err, PA_DEVERR_TIMEOUT);
+      if (!alive && lane == 0) raise_timeout(a.err, a.epoch);
       if (alive && i > i0) {
-        alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[grp], (unsigned)((i - 1) & 1), a.err));
+        alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[grp], (unsigned)((i - 1) & 1), a.err, a.epoch));
         tc_fence_after();
       }
       const bool have = alive && i > i0 && l_run != 0.f;

@@ -44,35 +44,53 @@ def test_version_and_status_strings(lib):
     assert lib.pa_status_string(pa.PA_ERANGE) != lib.pa_status_string(0)
 
 
-def test_options_validate(lib):
+def test_the_only_process_wide_option_is_checked_mode(lib):
     assert lib.pa_set_option(999, 1) == pa.PA_EINVAL
+    for legacy in range(2, 8):  # tuning and layout choices are per-call options now
+        assert lib.pa_set_option(legacy, 0) == pa.PA_EINVAL
+        assert lib.pa_get_option(legacy) == pa.PA_EINVAL
     assert lib.pa_set_option(pa.PA_OPT_CHECKED, 2) == pa.PA_EINVAL
-    assert lib.pa_set_option(pa.PA_OPT_DECODE_KERNEL, 3) == pa.PA_EINVAL
-    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 256) == 0
-    assert lib.pa_get_option(pa.PA_OPT_PARTITION_TOKENS) == 256
-    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 0) == 0
-    assert lib.pa_set_option(pa.PA_OPT_CLUSTER_MERGE, 2) == pa.PA_EINVAL
-    assert lib.pa_get_option(pa.PA_OPT_CLUSTER_MERGE) == 0
-    assert lib.pa_set_option(pa.PA_OPT_KV_LAYOUT, 2) == pa.PA_EINVAL
-    assert lib.pa_get_option(pa.PA_OPT_KV_LAYOUT) == pa.KV_LAYOUT_SEPARATE
+    assert lib.pa_set_checked_mode(2) == pa.PA_EINVAL
+    assert lib.pa_set_checked_mode(1) == 0
+    assert lib.pa_get_option(pa.PA_OPT_CHECKED) == 1
+    assert lib.pa_set_checked_mode(0) == 0
+    assert lib.pa_get_option(pa.PA_OPT_CHECKED) == 0
 
 
-def test_unified_layout_requires_v_to_be_the_v_half_of_block_0(lib):
-    """With unified K/V blocks the V view must start one K half after the K view; any other pair
-    of pointers is refused before anything is launched (the pointers are never dereferenced)."""
-    half = 16 * 2 * 64 * 2
+def _opts(**kw):
+    return ctypes.byref(pa.make_opts(**kw))
+
+
+def test_per_call_options_are_validated_before_any_launch(lib):
+    """Bad per-call options are refused before anything touches a device (the pointers are never
+    dereferenced)."""
+    block = 16 * 2 * 64 * 2
     k = 1 << 20
-    assert lib.pa_set_option(pa.PA_OPT_KV_LAYOUT, pa.KV_LAYOUT_UNIFIED) == 0
-    try:
-        assert lib.copy_blocks(k, k + 2 * half, 1 << 24, 1, 4, half, None) == pa.PA_EINVAL
-        assert lib.copy_blocks(k + half, k, 1 << 24, 1, 4, half, None) == pa.PA_EINVAL
-        assert lib.paged_kv_write(1 << 24, 1 << 24, 1 << 24, 1, k, k + 16, 4, 16, 2, 64, pa.PA_BF16, None) \
-            == pa.PA_EINVAL
-        args = [1 << 24, 1 << 24, k, k + half // 2, 1 << 24, 4, 1 << 24, 2, 8, 16, 1.0]
-        assert lib.paged_attention_decode(*args, 8, 2, 64, pa.PA_BF16, None, 0, None) == pa.PA_EINVAL
-        assert lib.swap_blocks(k, k + half, 4, k, k + 3 * half, 4, 1 << 24, 1, half, None) == pa.PA_EINVAL
-    finally:
-        assert lib.pa_set_option(pa.PA_OPT_KV_LAYOUT, pa.KV_LAYOUT_SEPARATE) == 0
+    bad = [dict(kv_block_stride_bytes=block + 8),  # not a multiple of 16
+           dict(kv_block_stride_bytes=block - 16),  # shorter than a block
+           dict(kv_block_stride_bytes=-32), dict(decode_kernel=3), dict(prefill_kernel=3),
+           dict(partition_tokens=-1), dict(partition_tokens=(1 << 30) + 1)]
+    dec = [1 << 24, 1 << 24, k, k + block, 1 << 24, 4, 1 << 24, 2, 8, 16, 1.0, 8, 2, 64, pa.PA_BF16, None, 0]
+    for kw in bad:
+        o = _opts(**kw)
+        assert lib.paged_attention_decode_ex(*dec, o, None) == pa.PA_EINVAL, kw
+        assert lib.paged_attention_decode_fused_ex(1 << 24, 1 << 24, 1 << 24, 1 << 24, 1 << 24, k, k + block, 1 << 24,
+                                                   4, 1 << 24, 2, 8, 16, 1.0, 8, 2, 64, pa.PA_BF16, None, 0, o,
+                                                   None) == pa.PA_EINVAL, kw
+        assert lib.paged_attention_prefill_ex(1 << 24, 1 << 24, 1 << 24, 4, k, k + block, 1 << 24, 4, 1 << 24, 2, 8,
+                                              16, 1.0, 8, 2, 64, pa.PA_BF16, o, None) == pa.PA_EINVAL, kw
+        assert lib.paged_attention_decode_workspace_size_ex(64, 256, 16, 32, 8, 128, o) == 0, kw
+    for kw in bad[:3]:
+        o = _opts(**kw)
+        assert lib.paged_kv_write_ex(1 << 24, 1 << 24, 1 << 24, 1, k, k + block, 4, 16, 2, 64, pa.PA_BF16, o,
+                                     None) == pa.PA_EINVAL, kw
+        assert lib.copy_blocks_ex(k, k + block, 1 << 24, 1, 4, block, o, None) == pa.PA_EINVAL, kw
+        assert lib.swap_blocks_ex(k, k + block, 4, k, k + block, 4, 1 << 24, 1, block, o, None) == pa.PA_EINVAL, kw
+    reserved = pa.PaOpts(0, 0, 0, 0, 1)
+    assert lib.paged_attention_decode_ex(*dec, ctypes.byref(reserved), None) == pa.PA_EINVAL
+    # a null options pointer is the defaults: batch 0 is a no-op
+    zero = [None, None, None, None, None, 4, None, 0, 8, 16, 1.0, 8, 2, 64, pa.PA_BF16, None, 0]
+    assert lib.paged_attention_decode_ex(*zero, None, None) == 0
 
 
 def test_argument_errors_are_returned_before_any_launch(lib):
@@ -102,45 +120,57 @@ def test_argument_errors_are_returned_before_any_launch(lib):
     assert lib.paged_attention_lse_merge(n, n, n, n, 4, 2, 80, pa.PA_BF16, n) == pa.PA_EUNSUPPORTED
 
 
-def test_workspace_size_follows_the_partition_plan(lib):
-    f = lib.paged_attention_decode_workspace_size
+def test_split_plan_follows_the_partition_rule(lib):
+    plan = pa.decode_split_plan
     # short tables never split
-    assert f(64, 8, 16, 32, 8, 128) == 0
-    # 4096-token tables at the default 1024-token partitions: 4 partitions of (128 + 2) floats
-    ws = f(64, 256, 16, 32, 8, 128)
-    assert ws >= 64 * 32 * 4 * 130 * 4
-    assert ws % 16 == 0
-    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 2048) == 0
-    assert f(64, 256, 16, 32, 8, 128) < ws
-    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 0) == 0
+    assert plan(64, 8, 16, 32, 8, 128) == (128, 1, 0)
+    # 4096-token tables at 1024-token partitions: 4 partitions of (128 + 2) floats per (sequence, head)
+    pt, mp, ws = plan(64, 256, 16, 32, 8, 128)
+    assert (pt, mp) == (1024, 4)
+    assert ws >= 64 * 32 * 4 * 130 * 4 and ws % 16 == 0
+    assert plan(64, 256, 16, 32, 8, 128, partition_tokens=2048)[2] < ws
+    # invalid sizes
+    pt, mp, wb = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_size_t(0)
+    args = (ctypes.byref(pt), ctypes.byref(mp), ctypes.byref(wb))
+    assert lib.pa_decode_split_plan(0, 256, 16, 32, 8, 128, 0, 152, *args) == pa.PA_EINVAL
+    assert lib.pa_decode_split_plan(64, 256, 16, 32, 8, 128, 0, 0, *args) == pa.PA_EINVAL
+    assert lib.pa_decode_split_plan(64, 256, 16, 30, 8, 128, 0, 152, *args) == pa.PA_EINVAL
+    assert lib.pa_decode_split_plan(64, 256, 16, 32, 8, 128, -4, 152, *args) == pa.PA_EINVAL
 
 
-def _expected_workspace(batch, stride, bs, hq, hkv, d, part=0):
-    """The documented split-K plan: automatic partitions give about one wave of 456 decode CTAs when
-    every row is as long as its table allows, clamped to [256, 1024] tokens and rounded up to the
-    block size; slots = partitions + 1; acc, max, sum and per-sequence slot counts, 16-byte aligned."""
+def _expected_plan(batch, stride, bs, hq, hkv, d, part=0, sms=152):
+    """The documented split-K plan: automatic partitions give about one wave of decode CTAs (SM
+    count x 3, x 2 for groups of 16 query heads) when every row is as long as its table allows,
+    clamped to [256, 1024] tokens and rounded up to the block size; the workspace holds acc, max and
+    sum per (sequence, query head, partition), each section 16-byte aligned."""
     max_len = stride * bs
     if part <= 0:
-        part = min(max(-(-batch * hkv * max_len // 456), 256), 1024)
+        target = sms * (2 if hq // hkv > 8 else 3)
+        part = min(max(-(-batch * hkv * max_len // target), 256), 1024)
     part = -(-part // bs) * bs
     if part >= max_len:
-        return 0
-    slots = -(-max_len // part) + 1
-    n = batch * hq * slots
+        return max_len, 1, 0
+    parts = -(-max_len // part)
+    n = batch * hq * parts
     up16 = lambda x: (x + 15) // 16 * 16
-    return n * d * 4 + 2 * up16(n * 4) + up16(batch * 4)
+    return part, parts, n * d * 4 + 2 * up16(n * 4)
 
 
 @pytest.mark.parametrize("shape", [(64, 256, 16, 32, 8, 128), (1, 128, 16, 12, 12, 64), (8, 128, 16, 12, 12, 64),
-                                   (4, 8192, 16, 32, 8, 128), (64, 8, 16, 32, 8, 128), (3, 40, 32, 16, 1, 64)])
-def test_automatic_split_plan(lib, shape):
-    f = lib.paged_attention_decode_workspace_size
-    assert f(*shape) == _expected_workspace(*shape)
-    assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 512) == 0
-    try:
-        assert f(*shape) == _expected_workspace(*shape, part=512)
-    finally:
-        assert lib.pa_set_option(pa.PA_OPT_PARTITION_TOKENS, 0) == 0
+                                   (4, 8192, 16, 32, 8, 128), (64, 8, 16, 32, 8, 128), (3, 40, 32, 16, 1, 64),
+                                   (2, 512, 16, 64, 4, 128), (1, 64, 16, 16, 1, 128)])
+@pytest.mark.parametrize("sms", [152, 148, 132, 20])
+def test_automatic_split_plan(lib, shape, sms):
+    assert pa.decode_split_plan(*shape, sm_count=sms) == _expected_plan(*shape, sms=sms)
+    assert pa.decode_split_plan(*shape, partition_tokens=512, sm_count=sms) == _expected_plan(*shape, part=512,
+                                                                                              sms=sms)
+
+
+def test_groups_of_sixteen_plan_for_two_ctas_per_sm(lib):
+    # 4 sequences x 4 KV heads x 16384 tokens = 262144 tokens: over 3 x 152 = 456 CTAs (groups of 8)
+    # that is 575 -> 576-token partitions; over 2 x 152 = 304 CTAs (groups of 16) 863 -> 864
+    assert pa.decode_split_plan(4, 1024, 16, 32, 4, 128)[0] == 576
+    assert pa.decode_split_plan(4, 1024, 16, 64, 4, 128)[0] == 864
 
 
 def test_binding_refuses_cpu_tensors(lib):

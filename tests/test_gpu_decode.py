@@ -30,24 +30,20 @@ def assert_close(gpu: torch.Tensor, ref: np.ndarray, dtype, what=""):
 
 
 @pytest.fixture(autouse=True)
-def _reset_options(cuda_lib):
+def _reset_checked_mode(cuda_lib):
     pa = cuda_lib
     yield
-    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 0)
-    pa.set_option(pa.PA_OPT_DECODE_KERNEL, 0)
-    pa.set_option(pa.PA_OPT_CHECKED, 0)
-    pa.set_option(pa.PA_OPT_CLUSTER_MERGE, 0)
-    pa.set_option(pa.PA_OPT_DECODE_GRID, 0)
+    pa.set_checked_mode(False)
     pa.device_error_flags(clear=True)
 
 
-def run_decode(pa, case, q=None, lens=None, kp=None, vp=None, workspace="auto"):
+def run_decode(pa, case, q=None, lens=None, kp=None, vp=None, workspace="auto", **opts):
     q = case.q if q is None else q
     lens = case.context_lens if lens is None else lens
     kp = case.k_pool.cuda() if kp is None else kp
     vp = case.v_pool.cuda() if vp is None else vp
     out = pa.paged_attention_decode(q.cuda(), kp, vp, case.block_table.cuda(), lens.cuda(), case.scale,
-                                    workspace=workspace)
+                                    workspace=workspace, **opts)
     torch.cuda.synchronize()
     return out
 
@@ -91,7 +87,7 @@ def test_kv_write_empty_and_out_of_range_slot(cuda_lib):
     assert pa.device_error_flags() & pa.PA_DEVERR_SLOT
     assert float(kp.view(-1, 2, 64)[5].float().min()) == 1.0
     assert float(kp.float().sum()) == 2 * 64  # nothing else written
-    pa.set_option(pa.PA_OPT_CHECKED, 1)
+    pa.set_checked_mode(True)
     with pytest.raises(pa.PagedAttnError) as ei:
         pa.paged_kv_write(kn, kn, slots, kp, vp)
     assert ei.value.status == pa.PA_ERANGE
@@ -121,7 +117,7 @@ def test_copy_blocks_bad_pair_is_flagged_not_faulted(cuda_lib):
     pa.copy_blocks(kp, vp, torch.tensor([[1, 2], [1, 9]], dtype=torch.int64, device="cuda"))
     assert pa.device_error_flags() & pa.PA_DEVERR_COPY_PAIR
     assert float(kp[2].float().min()) == 1.0
-    pa.set_option(pa.PA_OPT_CHECKED, 1)
+    pa.set_checked_mode(True)
     with pytest.raises(pa.PagedAttnError):
         pa.copy_blocks(kp, vp, torch.tensor([[1, 2], [3, 2]], dtype=torch.int64, device="cuda"))
 
@@ -160,29 +156,21 @@ def _ragged_case(dtype, Hq, Hkv, D, S, lens, seed, NB=None):
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("S", [8, 16, 32])
-@pytest.mark.parametrize("part", [0, 64, 128, "none", "cluster"])
+@pytest.mark.parametrize("part", [0, 64, 128, "none"])
 @pytest.mark.parametrize("kernel", [0, 1])
 def test_decode_shapes_and_partitions(cuda_lib, dtype, D, G, S, part, kernel):
     """kernel 0 = automatic choice (tensor-core path for bf16/fp16 with block_size % 16 == 0),
     1 = CUDA-core path forced.  part 64 gives 9-19 partitions per row, 128 gives 4-9 (workspace +
-    merge kernel); "cluster" = 128-token partitions with the thread-block-cluster merge switched on
-    (used on the tensor-core path when a row has at most 8 partitions)."""
+    merge kernel)."""
     pa = cuda_lib
-    pa.set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
-    if part == "cluster":
-        pa.set_option(pa.PA_OPT_CLUSTER_MERGE, 1)
-        part = 128
     Hkv = 2
     lens = [0, 1, S - 1, S, S + 1, 3 * S + 5, 200, 517]  # history before the new token
     case = _ragged_case(dtype, Hkv * G, Hkv, D, S, lens, seed=D * 31 + G * 7 + S)
-    if part == "none":
-        ws = None
-    else:
-        pa.set_option(pa.PA_OPT_PARTITION_TOKENS, part)
-        ws = "auto"
+    ws = None if part == "none" else "auto"
     dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
     pa.paged_kv_write(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), dk, dv)
-    out = run_decode(pa, case, kp=dk, vp=dv, workspace=ws)
+    out = run_decode(pa, case, kp=dk, vp=dv, workspace=ws, decode_kernel=kernel,
+                     partition_tokens=0 if part == "none" else part)
     kp1, vp1 = oracle.paged_kv_write(case.k_pool, case.v_pool, case.k_new, case.v_new, case.slot_mapping)
     ref = oracle.paged_decode(case.q, kp1, vp1, case.block_table, case.context_lens, case.scale)
     assert_close(out, ref, dtype, f"{dtype} D{D} G{G} S{S} part{part} kernel{kernel}")
@@ -190,64 +178,56 @@ def test_decode_shapes_and_partitions(cuda_lib, dtype, D, G, S, part, kernel):
 
 
 # history lengths of a ragged batch: empty, single-token, block-aligned and long sequences next to
-# each other, so that equal-work ranges start and end inside sequences, hold several short ones,
-# and long sequences meet many ranges
+# each other, so that partitions end inside and at the end of blocks and long sequences split into
+# many partitions
 RAGGED_HIST = [0, 3000, 0, 15, 16, 1, 2047, 0, 5, 700, 4000, 31, 32, 33, 1500, 0, 2, 1023, 1024, 1025]
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
-@pytest.mark.parametrize("grid", [0, 1])
 @pytest.mark.parametrize("part", [0, 16, 64, 512])
-def test_decode_grids_on_a_ragged_batch_with_empty_sequences(cuda_lib, dtype, grid, part):
-    """Both split-K grids of the tensor-core decode (0: one CTA per partition, 1: equal work per
-    warp) against the oracle.  Sequences with history 0 are given context 0 (zeros out); part
-    16 gives 16-token partitions (and equal-work ranges of a few tiles), so long sequences spread
-    over hundreds of split-K slots."""
+def test_decode_on_a_ragged_batch_with_empty_sequences(cuda_lib, dtype, part):
+    """The split-K tensor-core decode against the oracle.  Sequences with history 0 are given
+    context 0 (zeros out); part 16 gives 16-token partitions, so long sequences spread over hundreds
+    of partitions (the one-CTA-per-row merge)."""
     pa = cuda_lib
-    pa.set_option(pa.PA_OPT_DECODE_GRID, grid)
-    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, part)
     case = _ragged_case(dtype, 32, 8, 128, 16, RAGGED_HIST, seed=21 + part)
     lens = (case.context_lens - 1).clamp(min=0)  # history only: the new tokens are not written here
-    out = run_decode(pa, case, lens=lens)
+    out = run_decode(pa, case, lens=lens, partition_tokens=part)
     ref = oracle.paged_decode(case.q, case.k_pool, case.v_pool, case.block_table, lens, case.scale)
-    assert_close(out, ref, dtype, f"grid {grid} part {part}")
+    assert_close(out, ref, dtype, f"part {part}")
     empty = (lens == 0).nonzero().flatten()
     assert torch.equal(out.cpu()[empty].float(), torch.zeros_like(out.cpu()[empty].float()))
     assert pa.device_error_flags() == 0
 
 
 @pytest.mark.parametrize("G,D", [(1, 64), (2, 128), (4, 128), (8, 128), (8, 64), (16, 128), (16, 64)])
-def test_equal_work_grid_other_groups_and_head_dims(cuda_lib, G, D):
-    """The equal-work grid for every query-group size and head_dim."""
+def test_ragged_batch_other_groups_and_head_dims(cuda_lib, G, D):
+    """The ragged batch with 128-token partitions for every query-group size and head_dim."""
     pa = cuda_lib
-    pa.set_option(pa.PA_OPT_DECODE_GRID, 1)
-    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 128)
     Hkv = 4
     case = _ragged_case(torch.bfloat16, Hkv * G, Hkv, D, 32, RAGGED_HIST, seed=40 + G * 3 + D)
     dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
     pa.paged_kv_write(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), dk, dv)
-    out = run_decode(pa, case, kp=dk, vp=dv)
+    out = run_decode(pa, case, kp=dk, vp=dv, partition_tokens=128)
     kp1, vp1 = oracle.paged_kv_write(case.k_pool, case.v_pool, case.k_new, case.v_new, case.slot_mapping)
     ref = oracle.paged_decode(case.q, kp1, vp1, case.block_table, case.context_lens, case.scale)
     assert_close(out, ref, torch.bfloat16, f"G{G} D{D}")
     assert pa.device_error_flags() == 0
 
 
-@pytest.mark.parametrize("grid", [0, 1])
-def test_split_decode_is_deterministic_and_stale_workspace_safe(cuda_lib, grid):
+def test_split_decode_is_deterministic_and_stale_workspace_safe(cuda_lib):
     """Two calls on one workspace give the same bits, also after the workspace was filled with NaN
     and after a call on a different batch (no state is carried from call to call)."""
     pa = cuda_lib
-    pa.set_option(pa.PA_OPT_DECODE_GRID, grid)
-    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 64)
     case = _ragged_case(torch.bfloat16, 32, 8, 128, 16, RAGGED_HIST, seed=23)
     other = _ragged_case(torch.bfloat16, 32, 8, 128, 16, list(reversed(RAGGED_HIST)), seed=24)
-    nbytes = pa.decode_workspace_size(len(RAGGED_HIST), case.block_table.stride(0), 16, 32, 8, 128)
+    nbytes = pa.decode_workspace_size(len(RAGGED_HIST), case.block_table.stride(0), 16, 32, 8, 128,
+                                      partition_tokens=64)
     ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device="cuda").view(torch.uint8)
     lens = (case.context_lens - 1).clamp(min=0)  # history only: the new tokens are not written here
-    out1 = run_decode(pa, case, lens=lens, workspace=ws).cpu()
-    run_decode(pa, other, lens=(other.context_lens - 1).clamp(min=0), workspace=ws)
-    out2 = run_decode(pa, case, lens=lens, workspace=ws).cpu()
+    out1 = run_decode(pa, case, lens=lens, workspace=ws, partition_tokens=64).cpu()
+    run_decode(pa, other, lens=(other.context_lens - 1).clamp(min=0), workspace=ws, partition_tokens=64)
+    out2 = run_decode(pa, case, lens=lens, workspace=ws, partition_tokens=64).cpu()
     assert torch.equal(bits(out1), bits(out2))
     assert torch.isfinite(out1.float()).all()
 
@@ -260,16 +240,13 @@ def test_decode_group_of_16_query_heads(cuda_lib, dtype, D, part, kernel):
     """16 query heads per KV head: both row halves of the tensor-core kernel's mma tile hold
     heads (and the CUDA-core path, kernel 1 or fp32, its largest query group)."""
     pa = cuda_lib
-    pa.set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
-    ws = None
-    if part != "none":
-        pa.set_option(pa.PA_OPT_PARTITION_TOKENS, part)
-        ws = "auto"
+    ws = None if part == "none" else "auto"
     lens = [0, 1, 15, 16, 17, 200, 517, 1300]
     case = _ragged_case(dtype, 32, 2, D, 16, lens, seed=D + 16)
     dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
     pa.paged_kv_write(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), dk, dv)
-    out = run_decode(pa, case, kp=dk, vp=dv, workspace=ws)
+    out = run_decode(pa, case, kp=dk, vp=dv, workspace=ws, decode_kernel=kernel,
+                     partition_tokens=0 if part == "none" else part)
     kp1, vp1 = oracle.paged_kv_write(case.k_pool, case.v_pool, case.k_new, case.v_new, case.slot_mapping)
     ref = oracle.paged_decode(case.q, kp1, vp1, case.block_table, case.context_lens, case.scale)
     assert_close(out, ref, dtype, f"G16 {dtype} D{D} part{part} kernel{kernel}")
@@ -330,7 +307,7 @@ def test_bad_block_id_is_flagged_and_masked(cuda_lib):
     assert torch.isfinite(out.float()).all()
     ref = oracle.paged_decode(case.q[1:], case.k_pool, case.v_pool, case.block_table[1:], lens[1:], case.scale)
     assert_close(out[1:], ref, torch.float16)
-    pa.set_option(pa.PA_OPT_CHECKED, 1)
+    pa.set_checked_mode(True)
     with pytest.raises(pa.PagedAttnError) as ei:
         pa.paged_attention_decode(case.q.cuda(), case.k_pool.cuda(), case.v_pool.cuda(), table.cuda(),
                                   lens.cuda(), case.scale)
@@ -350,11 +327,10 @@ def test_nan_in_context_propagates_like_the_definition(cuda_lib):
 
 def test_tensor_core_path_refuses_unsupported_shapes(cuda_lib):
     pa = cuda_lib
-    pa.set_option(pa.PA_OPT_DECODE_KERNEL, 2)
     for dtype, S in ((torch.float32, 16), (torch.bfloat16, 8)):
         case = _ragged_case(dtype, 8, 2, 64, S, [20], seed=13)
         with pytest.raises(pa.PagedAttnError) as ei:
-            run_decode(pa, case)
+            run_decode(pa, case, decode_kernel=2)
         assert ei.value.status == pa.PA_EUNSUPPORTED
 
 
@@ -362,12 +338,11 @@ def test_tensor_core_path_refuses_unsupported_shapes(cuda_lib):
 def test_both_kernels_agree_on_the_serving_shape(cuda_lib, kernel):
     """CUDA-core and tensor-core decode on a reduced serving batch (8 sequences, 512-4096 tokens)."""
     pa = cuda_lib
-    pa.set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
     lens = W.llama_context_lens()[:8]
     case = _ragged_case(torch.bfloat16, 32, 8, 128, 16, [n - 1 for n in lens], seed=14)
     dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
     pa.paged_kv_write(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), dk, dv)
-    out = run_decode(pa, case, kp=dk, vp=dv)
+    out = run_decode(pa, case, kp=dk, vp=dv, decode_kernel=kernel)
     kp1, vp1 = oracle.paged_kv_write(case.k_pool, case.v_pool, case.k_new, case.v_new, case.slot_mapping)
     ref = oracle.paged_decode(case.q, kp1, vp1, case.block_table, case.context_lens, case.scale)
     assert_close(out, ref, torch.bfloat16, f"kernel {kernel}")
@@ -375,12 +350,11 @@ def test_both_kernels_agree_on_the_serving_shape(cuda_lib, kernel):
 
 def test_workspace_too_small_is_rejected(cuda_lib):
     pa = cuda_lib
-    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 128)  # 16 partitions: more than a cluster merges, workspace needed
     case = _ragged_case(torch.bfloat16, 8, 2, 64, 16, [2000], seed=10)
     with pytest.raises(pa.PagedAttnError) as ei:
         pa.paged_attention_decode(case.q.cuda(), case.k_pool.cuda(), case.v_pool.cuda(),
                                   case.block_table.cuda(), case.context_lens.cuda(), case.scale,
-                                  workspace=torch.empty(64, dtype=torch.uint8, device="cuda"))
+                                  workspace=torch.empty(64, dtype=torch.uint8, device="cuda"), partition_tokens=128)
     assert ei.value.status == pa.PA_EWORKSPACE
 
 

@@ -21,11 +21,7 @@ def bits(t):
 @pytest.fixture(autouse=True)
 def _reset(cuda_lib):
     yield
-    cuda_lib.set_option(cuda_lib.PA_OPT_DECODE_KERNEL, 0)
-    cuda_lib.set_option(cuda_lib.PA_OPT_PARTITION_TOKENS, 0)
-    cuda_lib.set_option(cuda_lib.PA_OPT_CHECKED, 0)
-    cuda_lib.set_option(cuda_lib.PA_OPT_CLUSTER_MERGE, 0)
-    cuda_lib.set_option(cuda_lib.PA_OPT_DECODE_GRID, 0)
+    cuda_lib.set_checked_mode(False)
     cuda_lib.device_error_flags(clear=True)
 
 
@@ -36,15 +32,16 @@ def _case(dtype, Hq, Hkv, D, S, lens, seed):
                          dtype=dtype, num_blocks=need + 5, max_blocks_per_seq=maxb)
 
 
-def _both(pa, case, workspace="auto"):
+def _both(pa, case, workspace="auto", **opts):
     dev = {k: getattr(case, k).cuda() for k in ("q", "k_new", "v_new", "slot_mapping", "block_table", "context_lens")}
     k1, v1 = case.k_pool.cuda(), case.v_pool.cuda()
     pa.paged_kv_write(dev["k_new"], dev["v_new"], dev["slot_mapping"], k1, v1)
     ref = pa.paged_attention_decode(dev["q"], k1, v1, dev["block_table"], dev["context_lens"], case.scale,
-                                    workspace=workspace)
+                                    workspace=workspace, **opts)
     k2, v2 = case.k_pool.cuda(), case.v_pool.cuda()
     out = pa.paged_attention_decode_fused(dev["q"], dev["k_new"], dev["v_new"], dev["slot_mapping"], k2, v2,
-                                          dev["block_table"], dev["context_lens"], case.scale, workspace=workspace)
+                                          dev["block_table"], dev["context_lens"], case.scale, workspace=workspace,
+                                          **opts)
     torch.cuda.synchronize()
     return out.cpu(), ref.cpu(), (k1.cpu(), v1.cpu()), (k2.cpu(), v2.cpu())
 
@@ -52,20 +49,12 @@ def _both(pa, case, workspace="auto"):
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("D,G,S", [(128, 4, 16), (64, 1, 16), (128, 8, 32), (64, 2, 8), (128, 16, 16)])
 @pytest.mark.parametrize("kernel", [0, 1])
-@pytest.mark.parametrize("split", [True, False, "cluster", "equal-work"])
+@pytest.mark.parametrize("split", [64, 128, None])
 def test_fused_equals_write_then_decode(cuda_lib, dtype, D, G, S, kernel, split):
     pa = cuda_lib
-    pa.set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
-    pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 64)
-    if split == "equal-work":
-        pa.set_option(pa.PA_OPT_DECODE_GRID, 1)
-        split = True
-    if split == "cluster":
-        pa.set_option(pa.PA_OPT_CLUSTER_MERGE, 1)
-        pa.set_option(pa.PA_OPT_PARTITION_TOKENS, 128)
-        split = True
     case = _case(dtype, 2 * G, 2, D, S, [0, 1, S - 1, S, 100, 777], seed=D + G + S)
-    out, ref, pools_a, pools_b = _both(pa, case, workspace="auto" if split else None)
+    out, ref, pools_a, pools_b = _both(pa, case, workspace="auto" if split else None, decode_kernel=kernel,
+                                       partition_tokens=split or 0)
     assert torch.equal(bits(out), bits(ref))
     assert torch.equal(bits(pools_a[0]), bits(pools_b[0])) and torch.equal(bits(pools_a[1]), bits(pools_b[1]))
     assert pa.device_error_flags() == 0
@@ -117,7 +106,7 @@ def test_slot_that_is_not_the_last_position_is_rejected(cuda_lib):
                                     case.block_table.cuda(), case.context_lens.cuda(), case.scale)
     assert pa.device_error_flags() & pa.PA_DEVERR_SLOT
     assert torch.equal(bits(dk.view(-1, 2, 64)[slot[1]].cpu()), bits(before.view(-1, 2, 64)[slot[1]].cpu()))
-    pa.set_option(pa.PA_OPT_CHECKED, 1)
+    pa.set_checked_mode(True)
     with pytest.raises(pa.PagedAttnError) as ei:
         pa.paged_attention_decode_fused(case.q.cuda(), case.k_new.cuda(), case.v_new.cuda(), slot.cuda(), dk, dv,
                                         case.block_table.cuda(), case.context_lens.cuda(), case.scale)

@@ -25,22 +25,21 @@ def assert_close(got: torch.Tensor, ref: np.ndarray, dtype, what=""):
 
 
 @pytest.fixture(autouse=True)
-def _reset_options(cuda_lib):
+def _reset_checked_mode(cuda_lib):
     yield
-    cuda_lib.set_option(cuda_lib.PA_OPT_PREFILL_KERNEL, 0)
-    cuda_lib.set_option(cuda_lib.PA_OPT_CHECKED, 0)
+    cuda_lib.set_checked_mode(False)
     cuda_lib.device_error_flags(clear=True)
 
 
 def run_case(pa, case, kernel=0):
-    pa.set_option(pa.PA_OPT_PREFILL_KERNEL, kernel)
     dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
     if case.copy_pairs.numel():
         pa.copy_blocks(dk, dv, case.copy_pairs.cuda())
     if case.slot_mapping.numel():
         pa.paged_kv_write(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), dk, dv)
     out = pa.paged_attention_prefill(case.q.cuda(), case.query_start_loc.cuda(), dk, dv,
-                                     case.block_table.cuda(), case.context_lens.cuda(), case.scale)
+                                     case.block_table.cuda(), case.context_lens.cuda(), case.scale,
+                                     prefill_kernel=kernel)
     torch.cuda.synchronize()
     return out.cpu(), dk, dv
 
@@ -56,12 +55,10 @@ def oracle_pools(case):
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 4, 8, 16])
 @pytest.mark.parametrize("S", [16, 32])
-@pytest.mark.parametrize("kernel", [0, 1, 3])
+@pytest.mark.parametrize("kernel", [0, 1])
 def test_prefill_ragged_chunks(cuda_lib, dtype, D, G, S, kernel):
-    """kernel 0 = automatic (tcgen05 path for bf16/fp16), 1 = CUDA cores, 3 = mma.sync path."""
+    """kernel 0 = automatic (tcgen05 path for bf16/fp16, CUDA cores for fp32), 1 = CUDA cores."""
     pa = cuda_lib
-    if kernel == 3 and dtype == torch.float32:
-        pytest.skip("the tensor-core paths take bf16/fp16 only (fp32 is covered by kernels 0 and 1)")
     case = W.varlen_prefill(D + G + S, hist_lens=[0, 5, 40, 17, 130, 0, 300], chunk_lens=[9, 0, 23, 1, 70, 64, 200],
                             block_size=S, n_q_heads=2 * G, n_kv_heads=2, head_dim=D, dtype=dtype,
                             num_blocks=96)
@@ -101,7 +98,7 @@ def test_prefill_many_items_per_cta(cuda_lib, G, D):
     assert pa.device_error_flags() == 0
 
 
-@pytest.mark.parametrize("kernel", [0, 3])
+@pytest.mark.parametrize("kernel", [0, 1])
 def test_prefill_cow_arm_small_equals_unshared_copy(cuda_lib, kernel):
     """Copy-on-write fork of a shared partial block: the forked sequences attend exactly like
     sequences that never shared (JuliaPagedAttn README, "Copy-on-Write")."""
@@ -133,22 +130,21 @@ def test_prefill_cow_arm_small_equals_unshared_copy(cuda_lib, kernel):
         kp.view(-1, 8, 128)[sl] = k_l
         vp.view(-1, 8, 128)[sl] = v_l
     out2 = pa.paged_attention_prefill(case.q.cuda(), case.query_start_loc.cuda(), kp.cuda(), vp.cuda(),
-                                      table.cuda(), case.context_lens.cuda(), case.scale).cpu()
+                                      table.cuda(), case.context_lens.cuda(), case.scale, prefill_kernel=kernel).cpu()
     assert torch.equal(bits(out), bits(out2))
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2])
 def test_prefill_bad_block_id_is_flagged(cuda_lib, kernel):
     pa = cuda_lib
     case = W.varlen_prefill(4, hist_lens=[40, 40], chunk_lens=[24, 24], block_size=16, n_q_heads=8, n_kv_heads=2,
                             head_dim=128, dtype=torch.bfloat16, num_blocks=16)
     table = case.block_table.clone()
     table[0, 1] = 999
-    pa.set_option(pa.PA_OPT_PREFILL_KERNEL, kernel)
     dk, dv = case.k_pool.cuda(), case.v_pool.cuda()
     pa.paged_kv_write(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), dk, dv)
     out = pa.paged_attention_prefill(case.q.cuda(), case.query_start_loc.cuda(), dk, dv, table.cuda(),
-                                     case.context_lens.cuda(), case.scale).cpu()
+                                     case.context_lens.cuda(), case.scale, prefill_kernel=kernel).cpu()
     assert pa.device_error_flags() & pa.PA_DEVERR_BLOCK_ID
     kp, vp = oracle_pools(case)
     res = oracle.paged_prefill(case.q, case.query_start_loc, kp, vp, case.block_table, case.context_lens,
@@ -159,7 +155,6 @@ def test_prefill_bad_block_id_is_flagged(cuda_lib, kernel):
 
 def test_prefill_tensor_core_refuses_unsupported(cuda_lib):
     pa = cuda_lib
-    pa.set_option(pa.PA_OPT_PREFILL_KERNEL, 2)
     case = W.varlen_prefill(5, hist_lens=[3], chunk_lens=[5], block_size=8, n_q_heads=4, n_kv_heads=2,
                             head_dim=64, dtype=torch.bfloat16, num_blocks=4)
     with pytest.raises(pa.PagedAttnError) as ei:
@@ -179,7 +174,7 @@ def test_prefill_bad_query_start_loc_is_flagged(cuda_lib):
     torch.cuda.synchronize()
     assert pa.device_error_flags() & pa.PA_DEVERR_QUERY_LOC
     assert torch.isfinite(out.float()).all()
-    pa.set_option(pa.PA_OPT_CHECKED, 1)
+    pa.set_checked_mode(True)
     with pytest.raises(pa.PagedAttnError):
         pa.paged_attention_prefill(case.q.cuda(), case.query_start_loc.cuda(), dk, dv, case.block_table.cuda(),
                                    lens.cuda(), case.scale)
@@ -196,10 +191,10 @@ def _sampled_check(case, out, seqs, rows_per_seq):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2])
 def test_prefill_shared_prefix_full(cuda_lib, kernel):
     """Chunked prefill, 128 sequences over a 1024-token shared prefix: sampled rows vs the oracle
-    (kernel 1 = CUDA cores, 2 = tcgen05 (the launch configuration bench.py times), 3 = mma.sync)."""
+    (kernel 1 = CUDA cores, 2 = tcgen05, the launch configuration bench.py times)."""
     pa = cuda_lib
     case = W.prefill_cow()
     out, _, _ = run_case(pa, case, kernel=kernel)
@@ -228,7 +223,7 @@ def test_prefill_cow_fork_full(cuda_lib):
         assert_close(out[qsl[b]:qsl[b + 1]][rows], ref[rows], torch.bfloat16, f"cow full seq {b}")
 
 
-@pytest.mark.parametrize("kernel", [0, 1, 3])
+@pytest.mark.parametrize("kernel", [0, 1])
 def test_mixed_decode_and_prefill_batch(cuda_lib, kernel):
     """The continuous-batching step: decode rows (1-query chunks at the last position) and prefill
     chunks of any length in one paged_attention_prefill launch; the decode rows also agree with

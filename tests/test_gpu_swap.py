@@ -19,7 +19,7 @@ def bits(t):
 @pytest.fixture(autouse=True)
 def _reset(cuda_lib):
     yield
-    cuda_lib.set_option(cuda_lib.PA_OPT_CHECKED, 0)
+    cuda_lib.set_checked_mode(False)
     cuda_lib.device_error_flags(clear=True)
 
 
@@ -104,7 +104,7 @@ def test_swap_errors(cuda_lib):
                          ctypes.c_void_p(torch.zeros((1, 2), dtype=torch.int64, device="cuda").data_ptr()), 1,
                          16 * 2 * 64 * 2, None)
     assert st == pa.PA_EINVAL
-    pa.set_option(pa.PA_OPT_CHECKED, 1)
+    pa.set_checked_mode(True)
     with pytest.raises(pa.PagedAttnError) as ei:
         pa.swap_blocks(k, v, hk, hv, torch.tensor([[1, 2], [3, 2]], dtype=torch.int64, device="cuda"))
     assert ei.value.status == pa.PA_ERANGE
