@@ -405,9 +405,26 @@ def _opts(pa, **kw):
     return ctypes.byref(pa.make_opts(**kw))
 
 
+class L2Flush:
+    """Evicts the L2 between timed launches: writes a buffer of ``nbytes`` (2x L2 by default), then
+    reads a second one of the same size, so that the write's dirty lines are written back here,
+    outside the timed region, and not while the next timed kernel streams its own data."""
+
+    def __init__(self, dev, nbytes=None):
+        if nbytes is None:
+            nbytes = 2 * torch.cuda.get_device_properties(dev).L2_cache_size
+        n = max(int(nbytes) // 4, 1)
+        self.wbuf = torch.empty(n, dtype=torch.float32, device=dev)
+        self.rbuf = torch.zeros(n, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def fill_(self, value):
+        self.wbuf.fill_(value)
+        torch.sum(self.rbuf, dim=0, out=self.sink)
+
+
 def _flush_buffer(dev):
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    return torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    return L2Flush(dev)
 
 
 def _check_device_flags(pa):
@@ -611,7 +628,7 @@ def run_cow(args):
         "config": {"workload": f"copy-on-write prefill step: {n_pairs} copy_blocks forks of the shared partial "
                                f"block (1000-token prefix, blocks of 32), paged_kv_write of {T} suffix + chunk "
                                "tokens, causal prefill of 128 chunks of 256 queries, 32q/8kv heads, head_dim 128",
-                   "l2": "L2 flushed (write of 2x L2) before each step; pools restored before each step (untimed)",
+                   "l2": "L2 flushed (write of 2x L2, then a read of 2x L2, so that the flush's dirty lines are written back before the timed region) before each step; pools restored before each step (untimed)",
                    "timing": "median per call over the steps, CUDA events between the calls"},
         "kernel_us": {"copy_blocks": med[0] * 1e3, "paged_kv_write": med[1] * 1e3, "prefill": med[2] * 1e3},
         "copy_blocks": {"pairs": n_pairs, "bytes": copy_bytes, "GB/s": copy_bytes / (med[0] * 1e-3) / 1e9,
@@ -672,7 +689,7 @@ def run_write(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) K/V, bf16)",
             "config": {"workload": f"paged_kv_write of the chunked-prefill chunk: {T} tokens x 8 KV heads x 128, "
                                    "block_size 32, 4096-block pool", "bytes_per_launch": nbytes,
-                       "l2": "L2 flushed (write of 2x L2) before each launch",
+                       "l2": "L2 flushed (write of 2x L2, then a read of 2x L2, so that the flush's dirty lines are written back before the timed region) before each launch",
                        "timing": "median of per-launch CUDA events"},
             "roofline": _roofline_hbm(gbs, peaks, kind, "kv_write_kernel", per_launch_bytes=nbytes),
             "gpu_launches": launches, "clocks": clk}
@@ -688,7 +705,7 @@ def _timed_fused_decode(pa, lib, *, lens, Hq, Hkv, Dh, S, dtype, code, pools_cou
                         warmup, seed, flush_bytes, graph=False, back_to_back=False):
     """Device time of one paged_attention_decode_fused call.  Per-call: the median of CUDA events around
     single calls that rotate through ``pools_count`` independent pools, with an L2 flush (a write
-    of ``flush_bytes``) before each call when that is non-zero.  ``back_to_back``: also the time per
+    of ``flush_bytes``, then a read of as many) before each call when that is non-zero.  ``back_to_back``: also the time per
     call of ``reps`` calls issued back to back (events only around the run, so programmatic
     dependent launch overlaps each call with the previous one).  ``graph``: also the median per call
     of a CUDA graph holding one call per pool (a captured layer loop), replayed ``reps`` times with
@@ -705,7 +722,7 @@ def _timed_fused_decode(pa, lib, *, lens, Hq, Hkv, Dh, S, dtype, code, pools_cou
     B = len(lens)
     ws_bytes = pa.decode_workspace_size(B, table.stride(0), S, Hq, Hkv, Dh)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    flush = torch.empty(max(flush_bytes // 4, 1), dtype=torch.float32, device=dev) if flush_bytes else None
+    flush = L2Flush(dev, flush_bytes) if flush_bytes else None
     scale = 1.0 / math.sqrt(Dh)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -821,8 +838,11 @@ def run_gpt2(args):
     clocks.start()
     clocks.mark("begin")
     launches0 = pa.launch_count()
+    only = set(args.gpt2_cells.split(",")) if args.gpt2_cells else None
     for bi, batch in enumerate(W.GPT2_BATCHES):
         for ci, context in enumerate(W.GPT2_CONTEXTS):
+            if only is not None and f"{batch}x{context}" not in only:
+                continue
             lens = [context] * batch
             need = batch * W.ceil_div(context, 16)
             r = _timed_fused_decode(pa, lib, lens=lens, Hq=12, Hkv=12, Dh=64, S=16, dtype=torch.float16,
@@ -852,12 +872,13 @@ def run_gpt2(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "fp16", "data": "synthetic (seeded N(0,1) Q/K/V, fp16)",
         "config": {"workload": "gpt2_small_decode_sweep: 12q = 12kv heads, head_dim 64, block_size 16, fp16, "
                                "batch {1,2,4,8} x context {128..2048}, 12 layer pools; value = batch 8 x 2048",
-                   "l2": "L2 flushed (write of 2x L2) before every timed single call or graph replay",
+                   "l2": "L2 flushed (write of 2x L2, then a read of 2x L2, so that the flush's dirty lines are written back before the timed region) before every timed single call or graph replay",
                    "timing": "median of per-call CUDA events; per call over back-to-back calls; per call in a "
                              "CUDA graph of the 12 layers' calls, replayed"},
         "cells": cells,
         "roofline": _roofline_hbm(big["GB/s"], peaks, kind,
-                                  "paged_attention_decode_fused at batch 8 x 2048 (50 MB per call)",
+                                  f"paged_attention_decode_fused at batch {big['batch']} x {big['context']} "
+                                  f"({big['bytes'] / 1e6:.1f} MB per call)",
                                   per_launch_bytes=big["bytes"]),
         "gpu_launches": launches, "clocks": clk,
     }
@@ -980,6 +1001,8 @@ def main():
                     default="decode")
     ap.add_argument("--unfused", action="store_true",
                     help="time paged_kv_write + paged_attention_decode as two calls instead of the fused call")
+    ap.add_argument("--gpt2-cells", default="",
+                    help="GPT-2 sweep: only these cells, e.g. 8x2048,1x128 (default: all 20)")
     ap.add_argument("--prefill-kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
     ap.add_argument("--kv-layout", choices=["separate", "unified"], default="separate",
                     help="separate K and V pools, or one pool of unified K/V blocks")

@@ -202,9 +202,10 @@ PA_API int paged_attention_decode_fused_ex(void* out, const void* q, const void*
 /*
  * Workspace bytes paged_attention_decode needs for split-K with these sizes on the current device
  * (0 if it never splits).  The split-K plan: a row (sequence, KV head) as long as its table allows
- * is cut into partitions of P tokens, P chosen so that the grid holds about one wave of decode
- * CTAs on this device (its SM count x 3 resident CTAs, x 2 for groups of 16 query heads), clamped
- * to [256, 1024] tokens and rounded up to block_size; rows no longer than P are not split.  The
+ * is cut into partitions of P tokens, P chosen so that the grid holds at most one wave of decode
+ * CTAs on this device (W = its SM count x 3 resident CTAs, x 2 for groups of 16 query heads): with
+ * R = batch x n_kv_heads rows, P = ceil(capacity / max(1, floor(W / R))), clamped to [256, 1024]
+ * tokens and rounded up to block_size; rows no longer than P are not split.  The
  * `_ex` form applies opts->partition_tokens instead when it is non-zero.  Invalid sizes give 0.
  */
 PA_API size_t paged_attention_decode_workspace_size(int batch, int64_t block_table_stride, int block_size,

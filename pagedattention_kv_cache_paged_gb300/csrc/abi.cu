@@ -171,8 +171,10 @@ int validate_tables(const int32_t* block_table, int64_t bt_stride, const int32_t
 }
 
 // Split-K plan: partition length in tokens and partitions per row.  The automatic length gives the
-// grid about one wave of the tensor-core decode (3 resident CTAs per SM, 2 for groups of 16 query
-// heads, times the device's SM count) when every row is as long as the table allows, between 256
+// grid at most one wave of the tensor-core decode (3 resident CTAs per SM, 2 for groups of 16 query
+// heads, times the device's SM count) when every row is as long as the table allows: each row gets
+// floor(wave / rows) partitions (at least one), so that rounding never spills a few CTAs into a
+// second wave that would take as long as the first.  The length stays between 256
 // tokens (four 16-token tiles per warp: below that the merge launch costs more than the shorter
 // partitions save) and 1024 (measured best at the serving shape, where rows are long and many:
 // shorter partitions there lose to per-CTA start-up and merge traffic).  Small batches of long rows
@@ -193,7 +195,8 @@ void plan_split(int batch, int n_kv_heads, int group, int sms, int64_t bt_stride
   if (p <= 0) {
     const int64_t target = split_target_ctas(sms, group);
     const int64_t rows = (int64_t)(batch > 0 ? batch : 1) * (n_kv_heads > 0 ? n_kv_heads : 1);
-    p = (rows * max_len + target - 1) / target;
+    const int64_t parts = target / rows > 1 ? target / rows : 1;
+    p = (max_len + parts - 1) / parts;
     p = p < 256 ? 256 : (p > 1024 ? 1024 : p);
   }
   p = ((p + block_size - 1) / block_size) * block_size;

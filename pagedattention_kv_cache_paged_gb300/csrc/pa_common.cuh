@@ -23,6 +23,14 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return r;
 }
 
+// 32-bit read-only load issued where it stands (not moved by the compiler), so that a value loaded
+// now and used much later has its latency hidden by the work in between.
+__device__ __forceinline__ int ld_nc_s32(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 // 2^x with the hardware approximation (ex2.approx; -inf -> +0).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

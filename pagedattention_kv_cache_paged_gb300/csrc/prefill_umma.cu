@@ -13,9 +13,13 @@
 //              S_k and O_k); turns each S_k tile into probabilities, rescales O_k in TMEM only when
 //              its stabilising maximum has to move up by more than 2^8, writes P_k (bf16/fp16) back
 //              into the TMEM columns of S_k, and normalises O_k at the end;
-//   warp 8     K producer: streams 128-key K tiles (TMA boxes of 16 keys x 64 columns from the
-//              physical blocks the table names) into a kUmKStages-deep ring and publishes which
-//              sub-tiles hold data;
+//   warp 8     K producer: finds each item's segments (the rows of one sequence: a binary search
+//              over query_start_loc and the length loads, dependent global loads that only this
+//              warp waits for, ahead of the others) and publishes the item's tile count (for the
+//              MMA warp) and a record per segment (for the V producer and the softmax groups)
+//              through small shared-memory rings; streams 128-key K tiles (TMA boxes of 16 keys x
+//              64 columns from the physical blocks the table names) into a kUmKStages-deep ring and
+//              publishes which sub-tiles hold data;
 //   warp 9     V producer: each item's two Q tiles (one TMA box per 64-column half, once the
 //              previous item's S products are done), then the matching V tiles into a
 //              kUmVStages-deep ring;
@@ -48,6 +52,8 @@ constexpr int kUmRows = 2 * kUmTileRows;    // rows per CTA
 constexpr int kUmKeys = 128;                // keys per K/V tile (N of S, K of PV)
 constexpr int kUmSub = kUmKeys / 16;
 constexpr int kUmTmemCols = 512;
+constexpr int kUmSegSlots = 8;   // segment records in flight between the K producer and their readers
+constexpr int kUmItemSlots = 4;  // item tile counts in flight between the K producer and the MMA warp
 // Ring depths (build-time overridable): K 2 / V 3 measured 1 % faster than K 3 / V 2 (V tiles are
 // needed later in a tile's chain, so their loads profit from the deeper ring)
 #ifndef PA_UM_KSTAGES
@@ -89,8 +95,17 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c, int half_bytes) {
 }
 
 // Softmax helpers: one thread owns one row of S (its TMEM lane); `taddr` is the row's first column.
-// Keys whose bit is clear in mask[q] (chunk q = columns 32q .. 32q + 31) are outside the causal
-// bound or were not loaded; kMasked = false is the common case of a tile with every key valid.
+//
+// One code path serves every tile.  The exponentials are taken as 2^(sc * s - m) with sc > 0, so
+// the row maximum can be taken over the raw scores and scaled once.  A tile that has masked keys
+// (outside the causal bound, or in a sub-tile that was not loaded), or a non-positive scale, first
+// rewrites the loaded scores in registers (ScoreFix): a masked key becomes -inf, whose probability
+// is exactly 0.  The common case, keys [0, nv) valid (the causal bound and the end of the loaded
+// keys both cut a prefix), costs one compare and select per key of the 64-key blocks that the cut
+// falls in, and a block wholly past the cut for every row of the warp is skipped.  Anything else
+// (a sub-tile skipped for an out-of-range block id, or a scale <= 0) takes the general rewrite: key c valid when bit c % 32 of mask[c / 32] is set, a negative scale flips
+// the sign of every score and uses |scale| (the same products sc * s), a zero scale makes every
+// score 0 with scale 1 (the same uniform weights).
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -98,120 +113,109 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// Columns [C0, C0 + N) of the row of S into registers: N / 32 loads in flight, one wait.
-template <int N, int C0>
-__device__ __forceinline__ void s_row_load(uint32_t taddr, uint32_t (&sv)[N]) {
-#pragma unroll
-  for (int q = 0; q < N / 32; ++q)
-    tmem_ld32(taddr + (uint32_t)(C0 + 32 * q), *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q]));
+// v = -inf unless j < nv (one compare, one select)
+__device__ __forceinline__ void keep_below(uint32_t& v, int j, int nv) {
+  asm("{\n\t.reg .pred p;\n\tsetp.lt.s32 p, %1, %2;\n\tselp.b32 %0, %0, 0xff800000, p;\n\t}"
+      : "+r"(v)
+      : "r"(j), "r"(nv));
+}
+
+struct ScoreFix {
+  int mode;       // 0: scores used as loaded; 1: keys >= nv masked; 2: general rewrite
+  int nv;         // mode 1: keys [0, nv) of the tile are valid
+  uint32_t flip;  // mode 2: sign bit flipped (negative scale)
+  bool zero;      // mode 2: scores replaced by 0 (zero scale)
+};
+
+// The softmax code runs once per tile on every SM; it is kept compact (one 64-column block in a
+// loop, not the whole row unrolled) so that it stays in the instruction cache: fully unrolled rows,
+// with a separate masked variant, measured slower from instruction fetch alone.
+
+// Columns [c0, c0 + 64) of the row of S into registers (two loads in flight, one wait), rewritten
+// as `fix` says; m0 / m1 are the mask words of the block's two 32-key chunks.  kGeneral = false
+// serves modes 0 and 1 with one copy of the code (the prefix cut is a short block behind a
+// warp-uniform branch, so a masked tile runs the instructions the unmasked ones keep in the
+// instruction cache); kGeneral = true is the rare mode 2.
+template <int kMode>
+__device__ __forceinline__ void s_load64(uint32_t taddr, uint32_t (&sv)[64], const ScoreFix& fix, int c0,
+                                         uint32_t m0, uint32_t m1) {
+  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+  tmem_ld32(taddr + 32u, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
   tmem_wait_ld();
+  tmem_pin32(*reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+  tmem_pin32(*reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+  if (kMode == 1) {
+    const int nv = fix.nv - c0;
+    if (nv < 64) {
 #pragma unroll
-  for (int q = 0; q < N / 32; ++q) tmem_pin32(*reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q]));
+      for (int j = 0; j < 64; ++j) keep_below(sv[j], j, nv);
+    }
+  } else if (kMode == 2) {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      const uint32_t v = fix.zero ? 0u : (sv[j] ^ fix.flip);
+      sv[j] = (((j < 32 ? m0 : m1) >> (j & 31)) & 1u) ? v : 0xff800000u;  // -inf
+    }
+  }
 }
 
-// Maximum of the scaled scores of keys [C0, C0 + N) (held in sv).  kMasked = false needs sc >= 0
-// (the maximum of the raw scores, scaled once).
-template <bool kMasked, int N, int C0>
-__device__ __forceinline__ float s_max(const uint32_t (&sv)[N], float sc, const uint32_t (&mask)[kUmKeys / 32]) {
+// Maximum of the 64 scores held in sv, times sc (> 0).
+__device__ __forceinline__ float s_max64(const uint32_t (&sv)[64], float sc) {
   float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  if (!kMasked) {
 #pragma unroll
-    for (int j = 0; j < N; j += 8)
+  for (int j = 0; j < 64; j += 8)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) m[u] = fmax3(m[u], __uint_as_float(sv[j + 2 * u]), __uint_as_float(sv[j + 2 * u + 1]));
-    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])) * sc;
-  }
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    const int k = C0 + j;
-    const float x = ((mask[k >> 5] >> (k & 31)) & 1u) ? __uint_as_float(sv[j]) * sc : -INFINITY;
-    m[j & 3] = fmaxf(m[j & 3], x);
-  }
-  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+    for (int u = 0; u < 4; ++u) m[u] = fmax3(m[u], __uint_as_float(sv[j + 2 * u]), __uint_as_float(sv[j + 2 * u + 1]));
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])) * sc;
 }
 
-// Probabilities 2^(sc * s - m_sub) of keys [C0, C0 + N) (0 for masked keys), written back as 16-bit
-// pairs into columns [C0 / 2, (C0 + N) / 2) of the row (keys 2c and 2c + 1 in column c); returns
-// their sum.  Those columns were read into registers before, so the stores overwrite nothing still
-// needed.
-template <bool kMasked, bool kBf16, int N, int C0>
-__device__ __forceinline__ float p_store(uint32_t taddr, const uint32_t (&sv)[N], float sc, float m_sub,
-                                         const uint32_t (&mask)[kUmKeys / 32]) {
-  static_assert(N % 64 == 0 && C0 % 64 == 0, "whole 32-column stores");
-  if (!kMasked) {
-    // packed pairs: one f32x2 fma for the scaled, shifted arguments and one f32x2 add for the sum
-    const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(-m_sub, -m_sub);
-    uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+// Probabilities 2^(sc * s - m_sub) of the 64 keys held in sv, written as 16-bit pairs into the 32
+// columns at taddr (keys 2c and 2c + 1 in column c); returns their sum.  Packed pairs: one f32x2 fma
+// for the scaled, shifted arguments and one f32x2 add for the sum.
+template <bool kBf16>
+__device__ __forceinline__ float p_store64(uint32_t taddr, const uint32_t (&sv)[64], float sc, float m_sub) {
+  const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(-m_sub, -m_sub);
+  uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+  uint32_t w[32];
 #pragma unroll
-    for (int h = 0; h < N / 64; ++h) {
-      uint32_t w[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int j = 64 * h + 2 * c;
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])), sc2, nm2), x0, x1);
-        const uint64_t e2 = f2_pack(fast_exp2(x0), fast_exp2(x1));
-        acc2[c & 1] = f2_add(acc2[c & 1], e2);
-        float e0, e1;
-        f2_unpack(e2, e0, e1);
-        w[c] = pack2<kBf16>(e0, e1);
-      }
-      tmem_st32(taddr + (uint32_t)(C0 / 2 + 32 * h), w);
-    }
-    float a0, a1, b0, b1;
-    f2_unpack(acc2[0], a0, a1);
-    f2_unpack(acc2[1], b0, b1);
-    return (a0 + b0) + (a1 + b1);
+  for (int c = 0; c < 32; ++c) {
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), sc2, nm2), x0, x1);
+    const uint64_t e2 = f2_pack(fast_exp2(x0), fast_exp2(x1));
+    acc2[c & 1] = f2_add(acc2[c & 1], e2);
+    float e0, e1;
+    f2_unpack(e2, e0, e1);
+    w[c] = pack2<kBf16>(e0, e1);
   }
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int h = 0; h < N / 64; ++h) {
-    uint32_t w[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int j = 64 * h + 2 * c;
-      const int k = C0 + j;
-      const uint32_t mq = mask[k >> 5];
-      float e0 = fast_exp2(fmaf(__uint_as_float(sv[j]), sc, -m_sub));
-      float e1 = fast_exp2(fmaf(__uint_as_float(sv[j + 1]), sc, -m_sub));
-      e0 = ((mq >> (k & 31)) & 1u) ? e0 : 0.f;
-      e1 = ((mq >> ((k + 1) & 31)) & 1u) ? e1 : 0.f;
-      acc[c & 3] += e0 + e1;
-      w[c] = pack2<kBf16>(e0, e1);
-    }
-    tmem_st32(taddr + (uint32_t)(C0 / 2 + 32 * h), w);
-  }
-  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  tmem_st32(taddr, w);
+  float a0, a1, b0, b1;
+  f2_unpack(acc2[0], a0, a1);
+  f2_unpack(acc2[1], b0, b1);
+  return (a0 + b0) + (a1 + b1);
 }
 
-// How the softmax reads a row of S: 1 = all kUmKeys columns with one wait (then the row stays in
-// registers for the exponentials), 2 = two halves for the maximum and the same two halves again
-// for the exponentials (half the registers, four waits).
-#ifndef PA_UM_ROW_SPLIT
-#define PA_UM_ROW_SPLIT 2
-#endif
-static_assert(PA_UM_ROW_SPLIT == 1 || PA_UM_ROW_SPLIT == 2, "row split");
-
-// Row maximum and probabilities of one S tile (see s_max / p_store); moves the stabilising maximum
-// m_use when it has to and returns the factor the earlier sum and O must be scaled by.
-template <bool kMasked, bool kBf16>
-__device__ __forceinline__ float row_softmax(uint32_t srow, float sc, const uint32_t (&mask)[kUmKeys / 32],
-                                             float& m_use, float& l_run) {
-  static_assert(kUmKeys == 128, "two halves of 64 keys");
-  float mx;
-#if PA_UM_ROW_SPLIT == 1
-  uint32_t sv[kUmKeys];
-  s_row_load<kUmKeys, 0>(srow, sv);
-  mx = s_max<kMasked, kUmKeys, 0>(sv, sc, mask);
-#else
-  {
+// Row maximum and probabilities of one S tile, in two blocks of 64 keys read twice (once for the
+// maximum, once for the exponentials, so that only 64 scores are held in registers at a time; the
+// P of block h goes to columns [32h, 32h + 32), which block h has already been read from).  Moves
+// the stabilising maximum m_use when it has to and returns the factor the earlier sum and O must be
+// scaled by.  sc > 0 (see ScoreFix).
+template <bool kBf16, int kMode>
+__device__ __forceinline__ float row_softmax(uint32_t srow, float sc, const ScoreFix& fix,
+                                             const uint32_t (&mask)[kUmKeys / 32], float& m_use, float& l_run) {
+  static_assert(kUmKeys == 128, "two blocks of 64 keys");
+  // a 64-key block masked for every row of the warp (past the causal cut or the loaded keys)
+  // contributes nothing: it is neither read nor exponentiated, its P is written as zeros
+  auto block_empty = [&](int h) {
+    return kMode == 1 && __all_sync(0xffffffffu, fix.nv - 64 * h <= 0);
+  };
+  float mx = -INFINITY;
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    if (block_empty(h)) continue;
     uint32_t sv[64];
-    s_row_load<64, 0>(srow, sv);
-    mx = s_max<kMasked, 64, 0>(sv, sc, mask);
-    s_row_load<64, 64>(srow, sv);
-    mx = fmaxf(mx, s_max<kMasked, 64, 64>(sv, sc, mask));
+    s_load64<kMode>(srow + 64u * h, sv, fix, 64 * h, h ? mask[2] : mask[0], h ? mask[3] : mask[1]);
+    mx = fmaxf(mx, s_max64(sv, sc));
   }
-#endif
   // move the stabiliser only when it must: first finite maximum, or growth beyond 2^8
   float corr = 1.f;
   if (mx > m_use + kUmRescaleThreshold || (m_use == -INFINITY && mx != -INFINITY)) {
@@ -219,32 +223,37 @@ __device__ __forceinline__ float row_softmax(uint32_t srow, float sc, const uint
     m_use = mx;
   }
   const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-#if PA_UM_ROW_SPLIT == 1
-  const float rs = p_store<kMasked, kBf16, kUmKeys, 0>(srow, sv, sc, m_sub, mask);
-#else
-  float rs;
-  {
+  float rs = 0.f;
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    if (block_empty(h)) {
+      uint32_t z[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) z[c] = 0u;
+      tmem_st32(srow + 32u * h, z);
+      continue;
+    }
     uint32_t sv[64];
-    s_row_load<64, 0>(srow, sv);
-    rs = p_store<kMasked, kBf16, 64, 0>(srow, sv, sc, m_sub, mask);
-    s_row_load<64, 64>(srow, sv);
-    rs += p_store<kMasked, kBf16, 64, 64>(srow, sv, sc, m_sub, mask);
+    s_load64<kMode>(srow + 64u * h, sv, fix, 64 * h, h ? mask[2] : mask[0], h ? mask[3] : mask[1]);
+    rs += p_store64<kBf16>(srow + 32u * h, sv, sc, m_sub);
   }
-#endif
   l_run = l_run * corr + rs;
   return corr;
 }
 
-// Sequence of query row t: the largest b < batch with qsl[b] <= t, searched by the whole warp with
-// 32 candidates per round (two rounds of loads for batch <= 1024).  Every lane gets the answer.
-__device__ __forceinline__ int find_sequence_warp(const int32_t* qsl, int batch, int t) {
-  const int lane = threadIdx.x & 31;
+// Sequence of query row t: the largest b < batch with qsl[b] <= t, searched by one thread with
+// rounds of 8 independent loads (three rounds for batch <= 512).
+__device__ __forceinline__ int find_sequence_8(const int32_t* qsl, int batch, int t) {
   int lo = 0, n = batch;
   while (n > 1) {
-    const int step = (n + 31) >> 5;
-    const bool le = lane * step < n && __ldg(qsl + lo + lane * step) <= t;
-    const unsigned m = __ballot_sync(0xffffffffu, le);
-    const int top = m ? 31 - __clz((int)m) : 0;
+    const int step = (n + 7) >> 3;
+    int v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = k * step < n ? ld_nc_s32(qsl + lo + k * step) : INT32_MAX;
+    int top = 0;
+#pragma unroll
+    for (int k = 1; k < 8; ++k)
+      if (k * step < n && v[k] <= t) top = k;
     const int nlo = lo + top * step;
     n = min(step, lo + n - nlo);
     lo = nlo;
@@ -277,12 +286,19 @@ __global__ void __launch_bounds__(kUmThreads)
   uint64_t* mready = bars + 24;   // [8] per tile slot: the sub-tile mask below is written
   uint64_t* q_empty = bars + 32;  // one phase per work item: its S products completed, Q may be reloaded
   uint64_t* o_free = bars + 33;   // [2] one phase per work item: group k has read O_k
+  uint64_t* seg_full = bars + 36;    // [kUmSegSlots] the record in the slot is written
+  uint64_t* seg_empty = bars + 44;   // [kUmSegSlots] the V producer and all 8 softmax warps have read it
+  uint64_t* item_full = bars + 52;   // [kUmItemSlots] the item's tile count is written
+  uint64_t* item_empty = bars + 56;  // [kUmItemSlots] the MMA warp has read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 512);
-  uint32_t* kmask = reinterpret_cast<uint32_t*>(base + 768);  // [8] sub-tiles holding data, per tile slot
+  int* item_tiles = reinterpret_cast<int*>(base + 516);       // [kUmItemSlots]
+  uint32_t* kmask = reinterpret_cast<uint32_t*>(base + 544);  // [8] sub-tiles holding data, per tile slot
+  int* seg_recs = reinterpret_cast<int*>(base + 576);         // [kUmSegSlots][8] segment records
   uint8_t* qs = base + 1024;                       // [2][Q tile]
   uint8_t* ks = qs + 2 * Cfg::kQBytes;             // [kUmKStages][K tile]
   uint8_t* vs = ks + kUmKStages * Cfg::kKvBytes;   // [kUmVStages][V tile]
   static_assert(kUmKStages <= 4 && kUmVStages <= 4, "barrier slots");
+  static_assert(576 + kUmSegSlots * 32 <= 1024 && 60 * 8 <= 512, "records and barriers fit their 1 KB slot");
 
   // Work items are (block of kQB query tokens, KV head) pairs; this CTA takes items blockIdx.x,
   // blockIdx.x + gridDim.x, ...  Query rows, positions and lengths all fit in int32
@@ -315,6 +331,14 @@ __global__ void __launch_bounds__(kUmThreads)
     }
     mbar_init(q_ready, 1);
     mbar_init(q_empty, 1);
+    for (int k = 0; k < kUmSegSlots; ++k) {
+      mbar_init(&seg_full[k], 1);
+      mbar_init(&seg_empty[k], 9);  // V producer, 8 softmax warps
+    }
+    for (int k = 0; k < kUmItemSlots; ++k) {
+      mbar_init(&item_full[k], 1);
+      mbar_init(&item_empty[k], 1);
+    }
     mbar_init(fin, 1);
     for (int s = 0; s < 8; ++s) mbar_init(&mready[s], 1);
     fence_barrier_init();
@@ -334,13 +358,10 @@ __global__ void __launch_bounds__(kUmThreads)
     int seg1, n, pos0, q0, kv_end;
     bool ok;
   };
-  // the rows [t, seg1) of rows [t, T1) that belong to the sequence holding row t (warp-collective)
-  auto segment_at = [&](int t, int T1) -> Seg {
+  // the rows [t, seg1) of rows [t, T1) that belong to sequence b (query rows [q0, q1), context
+  // length n), which holds row t
+  auto make_seg = [&](int t, int T1, int b, int q0, int q1, int n) -> Seg {
     Seg sg;
-    const int b = find_sequence_warp(a.query_start_loc, a.batch, t);
-    const int q0 = __ldg(a.query_start_loc + b);
-    const int q1 = __ldg(a.query_start_loc + b + 1);
-    int n = __ldg(a.context_lens + b);
     sg.b = b;
     sg.seg1 = min(q1, T1);
     if (sg.seg1 <= t) sg.seg1 = t + 1;
@@ -353,108 +374,256 @@ __global__ void __launch_bounds__(kUmThreads)
     return sg;
   };
   auto tiles_of = [](const Seg& sg) -> int { return (sg.kv_end + kUmKeys - 1) / kUmKeys; };
+  // Segment record idx of the K producer's stream, read by the whole warp, which then releases the
+  // slot (every reader releases a record as soon as it has read it, so the ring never holds up a
+  // reader the K producer waits for).  ok = false: the wait gave up (nothing is read).
+  auto seg_take = [&](int idx, bool& ok) -> Seg {
+    const int slot = idx % kUmSegSlots;
+    Seg sg{};
+    ok = __all_sync(0xffffffffu, mbar_wait(&seg_full[slot], (unsigned)((idx / kUmSegSlots) & 1), a.err, a.epoch));
+    if (ok) {
+      const int* rec = seg_recs + 8 * slot;
+      sg.b = rec[0];
+      sg.seg1 = rec[1];
+      sg.n = rec[2];
+      sg.pos0 = rec[3];
+      sg.q0 = rec[4];
+      sg.kv_end = rec[5];
+      sg.ok = rec[6] != 0;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&seg_empty[slot]);
+    return sg;
+  };
 
   if (warp == 8 || warp == 9) {
     // ------- producers: warp 8 streams K tiles; warp 9 each item's Q tiles, then its V tiles -------
-    const bool is_v = warp == 9;
-    uint64_t* full = is_v ? vfull : kfull;
-    uint64_t* empty = is_v ? vempty : kempty;
-    uint8_t* ring = is_v ? vs : ks;
-    const CUtensorMap* map = is_v ? &vmap : &kmap;
-    const int depth = is_v ? kUmVStages : kUmKStages;
-    int i = 0;      // tiles issued, counted over all items of the CTA
-    int nq = 0;     // Q loads issued
-    bool alive = true;
-    for (int w = blockIdx.x; w < n_items && alive; w += gridDim.x) {
-      const int kvh = w % a.n_kv_heads;
-      const int T0 = w / a.n_kv_heads * kQB;
-      const int T1 = min(T0 + kQB, rows);
-      if (is_v) {
-        // both Q tiles of the item, once every S product of the previous item has completed
-        bool ok = true;
-        if (lane == 0) {
-          ok = nq == 0 || mbar_wait(q_empty, (unsigned)((nq - 1) & 1), a.err, a.epoch);
-          if (ok) {
-            mbar_arrive_expect_tx(q_ready, 2 * Cfg::kQBytes);
+    // Each runs on lane 0 alone: a warp whose lanes meet at warp-collective steps between long
+    // single-lane stretches was measured to lose about a thousand cycles per meeting at item
+    // boundaries, so nothing here needs the other lanes.
+    if (lane == 0) {
+      const bool is_v = warp == 9;
+      uint64_t* full = is_v ? vfull : kfull;
+      uint64_t* empty = is_v ? vempty : kempty;
+      uint8_t* ring = is_v ? vs : ks;
+      const CUtensorMap* map = is_v ? &vmap : &kmap;
+      const int depth = is_v ? kUmVStages : kUmKStages;
+      int i = 0;      // tiles issued, counted over all items of the CTA
+      int nq = 0;     // Q loads issued
+      int rec = 0;    // segment records written (K) or read (V)
+      int nit = 0;    // item tile counts written (K)
+      bool alive = true;
+      // the segment of rows [t, T1) holding row t, looked up now
+      auto seg_lookup = [&](int t, int T1) -> Seg {
+        const int b = find_sequence_8(a.query_start_loc, a.batch, t);
+        return make_seg(t, T1, b, ld_nc_s32(a.query_start_loc + b), ld_nc_s32(a.query_start_loc + b + 1),
+                        ld_nc_s32(a.context_lens + b));
+      };
+      // K producer: the lookup of the next item's first segment runs one step per K tile of the
+      // current item (a round of 8 loads of the search over query_start_loc, then the loads of the
+      // sequence's bounds and length), each step's loads used by the next step, so that their
+      // latency passes while the warp waits for ring slots.  la_stage: 0 idle, 1 a search round in
+      // flight, 2 the final loads in flight, 3 done (la_seg holds the result).
+      int la_stage = 0, la_t = 0, la_T1 = 0, la_lo = 0, la_n = 0;
+      int la_v[8];
+      Seg la_seg{};
+      auto la_issue = [&]() {
+        if (la_n > 1) {
+          const int step = (la_n + 7) >> 3;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            la_v[k] = k * step < la_n ? ld_nc_s32(a.query_start_loc + la_lo + k * step) : INT32_MAX;
+          la_stage = 1;
+        } else {
+          la_v[0] = ld_nc_s32(a.query_start_loc + la_lo);
+          la_v[1] = ld_nc_s32(a.query_start_loc + la_lo + 1);
+          la_v[2] = ld_nc_s32(a.context_lens + la_lo);
+          la_stage = 2;
+        }
+      };
+      auto la_advance = [&]() {
+        if (la_stage == 1) {
+          const int step = (la_n + 7) >> 3;
+          int top = 0;
+#pragma unroll
+          for (int k = 1; k < 8; ++k)
+            if (k * step < la_n && la_v[k] <= la_t) top = k;
+          const int nlo = la_lo + top * step;
+          la_n = min(step, la_lo + la_n - nlo);
+          la_lo = nlo;
+          la_issue();
+        } else if (la_stage == 2) {
+          la_seg = make_seg(la_t, la_T1, la_lo, la_v[0], la_v[1], la_v[2]);
+          la_stage = 3;
+        }
+      };
+      for (int w = blockIdx.x; w < n_items && alive; w += gridDim.x) {
+        const int kvh = w % a.n_kv_heads;
+        const int T0 = w / a.n_kv_heads * kQB;
+        const int T1 = min(T0 + kQB, rows);
+        if (is_v) {
+          // both Q tiles of the item, once every S product of the previous item has completed; the
+          // CTA's next item's Q tiles are prefetched into L2 meanwhile
+          if (nq > 0 && !mbar_wait(q_empty, (unsigned)((nq - 1) & 1), a.err, a.epoch)) {
+            alive = false;
+            break;
+          }
+          mbar_arrive_expect_tx(q_ready, 2 * Cfg::kQBytes);
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int h = 0; h < kHalves; ++h)
+              tma_load_3d(qs + k * Cfg::kQBytes + h * Cfg::kQHalf, &qmap, h * 64, kvh * G,
+                          T0 + k * (kUmTileRows / G), q_ready);
+          const int wn = w + (int)gridDim.x;
+          if (wn < n_items) {
+            const int kvh_n = wn % a.n_kv_heads;
+            const int T0_n = wn / a.n_kv_heads * kQB;
 #pragma unroll
             for (int k = 0; k < 2; ++k)
 #pragma unroll
               for (int h = 0; h < kHalves; ++h)
-                tma_load_3d(qs + k * Cfg::kQBytes + h * Cfg::kQHalf, &qmap, h * 64, kvh * G,
-                            T0 + k * (kUmTileRows / G), q_ready);
+                tma_prefetch_3d(&qmap, h * 64, kvh_n * G, T0_n + k * (kUmTileRows / G));
           }
+          ++nq;
         }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          if (lane == 0) raise_timeout(a.err, a.epoch);
-          alive = false;
-          break;
-        }
-        ++nq;
-      }
-      for (int t = T0; t < T1 && alive;) {
-        const Seg sg = segment_at(t, T1);
-        const int32_t* table = a.block_table + (int64_t)sg.b * a.bt_stride;
-        const int nt = tiles_of(sg);
-        for (int tile = 0; tile < nt; ++tile, ++i) {
-          bool ok = true;
-          if (lane == 0) {
-            const int s = i % depth;
-            const int round = i / depth;
-            ok = round == 0 || mbar_wait(&empty[s], (unsigned)((round - 1) & 1), a.err, a.epoch);
-            if (ok) {
-              int ys[kUmSub], yo[kUmSub];
-              unsigned m = 0;
-#pragma unroll
-              for (int sub = 0; sub < kUmSub; ++sub) {
-                const int k0 = tile * kUmKeys + sub * 16;
-                ys[sub] = -1;
-                yo[sub] = 0;
-                if (k0 < sg.kv_end) {
-                  const int blk = __ldg(table + (k0 >> a.block_shift));
-                  if (blk < 0 || blk >= a.num_blocks) {
-                    if (!is_v) raise_error(a.err, PA_DEVERR_BLOCK_ID);
-                  } else {
-                    ys[sub] = blk;
-                    yo[sub] = k0 & bmask;
-                    m |= 1u << sub;
-                  }
-                }
-              }
-              if (!is_v) {
-                // publish which sub-tiles hold data; the softmax groups read it instead of the
-                // table.  Slot i % 8 was last read for tile i - 8, which both groups finished long
-                // ago: K tile i is loaded only after both S products of tile i - kUmKStages
-                // completed, which needed each group's P of tile i - kUmKStages - 1.
-                kmask[i & 7] = m;
-                mbar_arrive(&mready[i & 7]);
-              }
-              uint8_t* st = ring + s * Cfg::kKvBytes;
-              if (m == 0) {
-                mbar_arrive(&full[s]);
-              } else {
-                mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(m) * kHalves * 2048u);
-#pragma unroll
-                for (int sub = 0; sub < kUmSub; ++sub) {
-                  if (ys[sub] < 0) continue;
-#pragma unroll
-                  for (int h = 0; h < kHalves; ++h)
-                    tma_load_3d(st + h * Cfg::kKvHalf + sub * 2048, map, kvh * D + h * 64, yo[sub], ys[sub], &full[s]);
-                }
-              }
-            }
+        Seg first{};
+        if (!is_v) {
+          // the item's segments: first its tile count for the MMA warp (the first segment was
+          // looked up during the previous item)
+          if (la_stage != 0 && la_t == T0) {
+            while (la_stage != 3) la_advance();
+            first = la_seg;
+          } else {
+            first = seg_lookup(T0, T1);
           }
-          if (!__shfl_sync(0xffffffffu, ok, 0)) {
-            if (lane == 0) raise_timeout(a.err, a.epoch);
+          la_stage = 0;
+          int n_all = tiles_of(first);
+          for (int t = first.seg1; t < T1;) {
+            const Seg sg = seg_lookup(t, T1);
+            n_all += tiles_of(sg);
+            t = sg.seg1;
+          }
+          const int slot = nit % kUmItemSlots;
+          if (nit >= kUmItemSlots &&
+              !mbar_wait(&item_empty[slot], (unsigned)((nit / kUmItemSlots - 1) & 1), a.err, a.epoch)) {
             alive = false;
             break;
           }
+          item_tiles[slot] = n_all;
+          mbar_arrive(&item_full[slot]);
+          ++nit;
+          const int wn = w + (int)gridDim.x;
+          if (wn < n_items) {
+            la_t = wn / a.n_kv_heads * kQB;
+            la_T1 = min(la_t + kQB, rows);
+            la_lo = 0;
+            la_n = a.batch;
+            la_issue();
+          }
         }
-        t = sg.seg1;
+        for (int t = T0; t < T1 && alive;) {
+          Seg sg;
+          const int slot = rec % kUmSegSlots;
+          if (is_v) {
+            if (!mbar_wait(&seg_full[slot], (unsigned)((rec / kUmSegSlots) & 1), a.err, a.epoch)) {
+              alive = false;
+              break;
+            }
+            const int* r = seg_recs + 8 * slot;
+            sg.b = r[0];
+            sg.seg1 = r[1];
+            sg.n = r[2];
+            sg.pos0 = r[3];
+            sg.q0 = r[4];
+            sg.kv_end = r[5];
+            sg.ok = r[6] != 0;
+            mbar_arrive(&seg_empty[slot]);
+          } else {
+            // then each segment's record, for the V producer and the softmax groups
+            sg = t == T0 ? first : seg_lookup(t, T1);
+            if (rec >= kUmSegSlots &&
+                !mbar_wait(&seg_empty[slot], (unsigned)((rec / kUmSegSlots - 1) & 1), a.err, a.epoch)) {
+              alive = false;
+              break;
+            }
+            int* r = seg_recs + 8 * slot;
+            r[0] = sg.b;
+            r[1] = sg.seg1;
+            r[2] = sg.n;
+            r[3] = sg.pos0;
+            r[4] = sg.q0;
+            r[5] = sg.kv_end;
+            r[6] = sg.ok ? 1 : 0;
+            mbar_arrive(&seg_full[slot]);
+          }
+          ++rec;
+          const int32_t* table = a.block_table + (int64_t)sg.b * a.bt_stride;
+          const int nt = tiles_of(sg);
+          // the table entries of a tile's 16-key sub-tiles (-1: past the segment's keys), read one
+          // tile ahead so that their latency passes during the wait for the ring slot
+          int ys[kUmSub];
+          auto table_of = [&](int tile, int (&dst)[kUmSub]) {
+#pragma unroll
+            for (int sub = 0; sub < kUmSub; ++sub) {
+              const int k0 = tile * kUmKeys + sub * 16;
+              dst[sub] = k0 < sg.kv_end ? ld_nc_s32(table + (k0 >> a.block_shift)) : -1;
+            }
+          };
+          if (nt > 0) table_of(0, ys);
+          for (int tile = 0; tile < nt; ++tile, ++i) {
+            int ys_next[kUmSub];
+            if (tile + 1 < nt) table_of(tile + 1, ys_next);
+            const int s = i % depth;
+            const int round = i / depth;
+            if (round > 0 && !mbar_wait(&empty[s], (unsigned)((round - 1) & 1), a.err, a.epoch)) {
+              alive = false;
+              break;
+            }
+            unsigned m = 0;
+#pragma unroll
+            for (int sub = 0; sub < kUmSub; ++sub) {
+              const int k0 = tile * kUmKeys + sub * 16;
+              if (k0 < sg.kv_end) {
+                if (ys[sub] < 0 || ys[sub] >= a.num_blocks) {
+                  if (!is_v) raise_error(a.err, PA_DEVERR_BLOCK_ID);
+                } else {
+                  m |= 1u << sub;
+                }
+              }
+            }
+            if (!is_v) {
+              // publish which sub-tiles hold data; the softmax groups read it instead of the
+              // table.  Slot i % 8 was last read for tile i - 8, which both groups finished long
+              // ago: K tile i is loaded only after both S products of tile i - kUmKStages
+              // completed, which needed each group's P of tile i - kUmKStages - 1.
+              kmask[i & 7] = m;
+              mbar_arrive(&mready[i & 7]);
+            }
+            uint8_t* st = ring + s * Cfg::kKvBytes;
+            if (m == 0) {
+              mbar_arrive(&full[s]);
+            } else {
+              mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(m) * kHalves * 2048u);
+#pragma unroll
+              for (int sub = 0; sub < kUmSub; ++sub) {
+                if (!((m >> sub) & 1u)) continue;
+                const int yo = (tile * kUmKeys + sub * 16) & bmask;
+#pragma unroll
+                for (int h = 0; h < kHalves; ++h)
+                  tma_load_3d(st + h * Cfg::kKvHalf + sub * 2048, map, kvh * D + h * 64, yo, ys[sub], &full[s]);
+              }
+            }
+            if (!is_v) la_advance();
+#pragma unroll
+            for (int sub = 0; sub < kUmSub; ++sub) ys[sub] = ys_next[sub];
+          }
+          t = sg.seg1;
+        }
       }
-    }
-    // Leave no copy in flight: after a normal run every issued tile was consumed and these waits
-    // return at once; after a timeout elsewhere they wait (bounded) for this ring's last tiles.
-    if (lane == 0) {
+      if (!alive) raise_timeout(a.err, a.epoch);
+      // Leave no copy in flight: after a normal run every issued tile was consumed and these waits
+      // return at once; after a timeout elsewhere they wait (bounded) for this ring's last tiles.
       for (int k = i > depth ? i - depth : 0; k < i; ++k) mbar_wait(&full[k % depth], (unsigned)((k / depth) & 1));
       if (nq > 0) mbar_wait(q_ready, (unsigned)((nq - 1) & 1));
     }
@@ -483,20 +652,21 @@ __global__ void __launch_bounds__(kUmThreads)
                 (!first || kk > 0) ? 1u : 0u);
       umma_commit(&pv_done[k]);
     };
+    // lane 0 alone issues (no warp-collective step, as for the producers)
     int g = 0;  // tiles of earlier items
     int n = 0;  // items done
-    bool alive = true;
+    bool alive = lane == 0;
     for (int w = blockIdx.x; w < n_items && alive; w += gridDim.x, ++n) {
-      const int T0 = w / a.n_kv_heads * kQB;
-      const int T1 = min(T0 + kQB, rows);
+      // the item's tile count, from the K producer
       int n_all = 0;
-      for (int t = T0; t < T1;) {
-        const Seg sg = segment_at(t, T1);
-        n_all += tiles_of(sg);
-        t = sg.seg1;
-      }
       bool ok = true;
-      if (lane == 0) {
+      {
+        const int slot = n % kUmItemSlots;
+        ok = mbar_wait(&item_full[slot], (unsigned)((n / kUmItemSlots) & 1), a.err, a.epoch);
+        if (ok) n_all = item_tiles[slot];
+        mbar_arrive(&item_empty[slot]);
+      }
+      if (ok) {
         auto wait = [&](uint64_t* bar, unsigned parity) {
           ok = ok && mbar_wait(bar, parity, a.err, a.epoch);
           return ok;
@@ -544,7 +714,7 @@ __global__ void __launch_bounds__(kUmThreads)
         own_o(0);  // an item without tiles still takes its turn of both O buffers
         own_o(1);
       }
-      alive = __shfl_sync(0xffffffffu, ok, 0);
+      alive = ok;
       g += n_all;
     }
     if (lane == 0) {
@@ -560,7 +730,8 @@ __global__ void __launch_bounds__(kUmThreads)
     const int r = threadIdx.x & 127;     // row inside the Q tile = TMEM lane
     const int row = grp * kUmTileRows + r;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    int i = 0;  // tiles of this CTA so far
+    int i = 0;    // tiles of this CTA so far
+    int rec = 0;  // segment records read
     bool alive = true;
     for (int w = blockIdx.x; w < n_items && alive; w += gridDim.x) {
       const int kvh = w % a.n_kv_heads;
@@ -572,7 +743,12 @@ __global__ void __launch_bounds__(kUmThreads)
       float m_use = -INFINITY;  // stabilising maximum (log2 domain) the exponentials are taken against
       float l_run = 0.f;
       for (int t = T0; t < T1 && alive;) {
-        const Seg sg = segment_at(t, T1);
+        bool got = true;
+        const Seg sg = seg_take(rec++, got);
+        if (!got) {
+          alive = false;
+          break;
+        }
         if (!sg.ok && threadIdx.x == 0) raise_error(a.err, PA_DEVERR_QUERY_LOC);
         const int bound = (sg.ok && tok >= t && tok < sg.seg1) ? sg.pos0 + (tok - sg.q0) : -1;
         const int nt = tiles_of(sg);
@@ -608,12 +784,25 @@ __global__ void __launch_bounds__(kUmThreads)
             }
           }
           const uint32_t srow = tS(grp) + lane_base;
-          const float corr = (unmasked && sc >= 0.f) ? row_softmax<false, kBf16>(srow, sc, mask, m_use, l_run)
-                                                     : row_softmax<true, kBf16>(srow, sc, mask, m_use, l_run);
+          ScoreFix fix;
+          {
+            const int lim = bound - kb;  // keys c <= lim are causal
+            const int nvc = lim < 0 ? 0 : (lim >= kUmKeys ? kUmKeys : lim + 1);
+            const int nvl = 16 * __popc(loaded);
+            const bool prefix = (loaded & (loaded + 1u)) == 0u;  // the loaded sub-tiles are 0 .. k-1
+            fix.mode = (unmasked && sc > 0.f) ? 0 : ((prefix && sc > 0.f) ? 1 : 2);
+            fix.nv = nvc < nvl ? nvc : nvl;
+            fix.flip = sc < 0.f ? 0x80000000u : 0u;
+            fix.zero = sc == 0.f;
+          }
+          const float sc_pos = sc > 0.f ? sc : (sc < 0.f ? -sc : 1.f);
+          const float corr = fix.mode == 0   ? row_softmax<kBf16, 0>(srow, sc_pos, fix, mask, m_use, l_run)
+                             : fix.mode == 1 ? row_softmax<kBf16, 1>(srow, sc_pos, fix, mask, m_use, l_run)
+                                             : row_softmax<kBf16, 2>(srow, sc_pos, fix, mask, m_use, l_run);
           // O_k is stable here (its last product completed before this S_k was issued); the item's
           // first tile starts O_k afresh, so only later tiles rescale it
           if (i > i0 && __any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll
+#pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
               uint32_t v[32];
               tmem_ld32_sync(tO(grp) + lane_base + c0, v);
@@ -652,7 +841,7 @@ __global__ void __launch_bounds__(kUmThreads)
       const bool have = alive && i > i0 && l_run != 0.f;
       const float inv = have ? 1.f / l_run : 0.f;
       T* orow = static_cast<T*>(a.out) + ((int64_t)tok * a.n_q_heads + head) * D;
-#pragma unroll
+#pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[32];
         tmem_ld32_sync(tO(grp) + lane_base + c0, v);

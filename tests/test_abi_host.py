@@ -139,14 +139,16 @@ def test_split_plan_follows_the_partition_rule(lib):
 
 
 def _expected_plan(batch, stride, bs, hq, hkv, d, part=0, sms=152):
-    """The documented split-K plan: automatic partitions give about one wave of decode CTAs (SM
-    count x 3, x 2 for groups of 16 query heads) when every row is as long as its table allows,
-    clamped to [256, 1024] tokens and rounded up to the block size; the workspace holds acc, max and
-    sum per (sequence, query head, partition), each section 16-byte aligned."""
+    """The documented split-K plan: automatic partitions give at most one wave of decode CTAs (SM
+    count x 3, x 2 for groups of 16 query heads) when every row is as long as its table allows —
+    floor(wave / rows) partitions per row, at least one — clamped to [256, 1024] tokens and rounded
+    up to the block size; the workspace holds acc, max and sum per (sequence, query head,
+    partition), each section 16-byte aligned."""
     max_len = stride * bs
     if part <= 0:
         target = sms * (2 if hq // hkv > 8 else 3)
-        part = min(max(-(-batch * hkv * max_len // target), 256), 1024)
+        per_row = max(1, target // (batch * hkv))
+        part = min(max(-(-max_len // per_row), 256), 1024)
     part = -(-part // bs) * bs
     if part >= max_len:
         return max_len, 1, 0
@@ -167,10 +169,22 @@ def test_automatic_split_plan(lib, shape, sms):
 
 
 def test_groups_of_sixteen_plan_for_two_ctas_per_sm(lib):
-    # 4 sequences x 4 KV heads x 16384 tokens = 262144 tokens: over 3 x 152 = 456 CTAs (groups of 8)
-    # that is 575 -> 576-token partitions; over 2 x 152 = 304 CTAs (groups of 16) 863 -> 864
-    assert pa.decode_split_plan(4, 1024, 16, 32, 4, 128)[0] == 576
-    assert pa.decode_split_plan(4, 1024, 16, 64, 4, 128)[0] == 864
+    # 4 sequences x 4 KV heads = 16 rows of 16384 tokens: 3 x 152 = 456 CTAs (groups of 8) give 28
+    # partitions per row, 586 -> 592 tokens; 2 x 152 = 304 CTAs (groups of 16) give 19, 863 -> 864
+    assert pa.decode_split_plan(4, 1024, 16, 32, 4, 128)[:2] == (592, 28)
+    assert pa.decode_split_plan(4, 1024, 16, 64, 4, 128)[:2] == (864, 19)
+
+
+@pytest.mark.parametrize("shape", [(8, 128, 16, 12, 12, 64), (4, 1024, 16, 32, 4, 128), (3, 333, 16, 32, 8, 128),
+                                   (5, 999, 16, 40, 8, 128), (1, 8192, 16, 32, 8, 128)])
+def test_automatic_plan_never_spills_into_a_second_wave(lib, shape):
+    # a grid of rows x partitions that exceeded one wave by a few CTAs would run a second, nearly
+    # empty wave as long as the first (batch 8 x 2048 tokens at 12 heads: 5 partitions of 432 tokens
+    # made 480 CTAs for 456 slots; 4 of 512 make 384)
+    batch, hkv = shape[0], shape[4]
+    part, parts, _ = pa.decode_split_plan(*shape, sm_count=152)
+    if part > 256 and part < 1024:
+        assert batch * hkv * parts <= 152 * 3
 
 
 def test_binding_refuses_cpu_tensors(lib):
