@@ -41,13 +41,21 @@ HQ, HKV, D, S = 32, 8, 128, 16
 SEED_LONG = 1004  # seed of the long-context configuration's device inputs
 LLAMA_LAYERS = 32
 ELT = 2  # bf16
-# dram__bytes_read.sum + dram__bytes_write.sum of one paged_attention_decode_fused call on this
-# workload (partition kernel + merge kernel, mean of two calls with the cold L2 of the capture),
-# from one ncu capture of those metrics on the current kernels.  Retake it whenever either kernel
-# changes; None = not taken for the current kernels.
-FUSED_CALL_DRAM_BYTES = None
-# The same for one tcgen05 prefill launch on the chunked-prefill workload.
-PREFILL_DRAM_BYTES = None
+# dram__bytes_read.sum + dram__bytes_write.sum per launch (or per call of several launches) from one
+# ncu capture of those metrics on the current kernels (mean of the captured launches, with the
+# capture's cold L2).  Retake them whenever a kernel changes; None = not taken for the current
+# kernels.  Serving decode: one paged_attention_decode_fused call (partition + merge kernels).
+FUSED_CALL_DRAM_BYTES = 585.72e6
+# one tcgen05 prefill launch on the chunked-prefill workload
+PREFILL_DRAM_BYTES = 791.66e6
+# one decode call (partition + merge) of the GPT-2-shaped batch 8 x 2048 cell
+GPT2_8X2048_DRAM_BYTES = 50.52e6
+# one paged_kv_write launch of the 32,768-token prefill chunk (the written lines still in L2 when
+# the launch ends are written back after it, so the write bytes fall short of the 134 MB written)
+WRITE_CHUNK_DRAM_BYTES = 219.82e6
+# the copy-on-write step's copy_blocks launch (127 forks of one shared block) and its paged_kv_write
+COW_COPY_DRAM_BYTES = 0.147e6
+COW_WRITE_DRAM_BYTES = 495.71e6
 
 
 def measured_peaks():
@@ -632,9 +640,13 @@ def run_cow(args):
                    "timing": "median per call over the steps, CUDA events between the calls"},
         "kernel_us": {"copy_blocks": med[0] * 1e3, "paged_kv_write": med[1] * 1e3, "prefill": med[2] * 1e3},
         "copy_blocks": {"pairs": n_pairs, "bytes": copy_bytes, "GB/s": copy_bytes / (med[0] * 1e-3) / 1e9,
-                        "frac_hbm": copy_bytes / (med[0] * 1e-3) / 1e9 / float(peaks["hbm_gbs"])},
+                        "frac_hbm": copy_bytes / (med[0] * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
+                        "traffic": COW_COPY_DRAM_BYTES,
+                        "note": "every fork copies the same shared block (L2-resident after the first): "
+                                "launch-latency bound, DRAM traffic far below the bytes copied"},
         "paged_kv_write": {"tokens": T, "bytes": write_bytes, "GB/s": write_bytes / (med[1] * 1e-3) / 1e9,
-                           "frac_hbm": write_bytes / (med[1] * 1e-3) / 1e9 / float(peaks["hbm_gbs"])},
+                           "frac_hbm": write_bytes / (med[1] * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
+                           "traffic": COW_WRITE_DRAM_BYTES},
         "roofline": {"bound": "tensor", "kernel": "paged_attention_prefill (tcgen05)", "achieved": tflops,
                      "peak": float(peaks["bf16_tflops"]), "peak_kind": f"{kind} bf16 dense (burst)",
                      "unit": "TFLOP/s", "frac": tflops / float(peaks["bf16_tflops"]), "traffic": None},
@@ -691,7 +703,8 @@ def run_write(args):
                                    "block_size 32, 4096-block pool", "bytes_per_launch": nbytes,
                        "l2": "L2 flushed (write of 2x L2, then a read of 2x L2, so that the flush's dirty lines are written back before the timed region) before each launch",
                        "timing": "median of per-launch CUDA events"},
-            "roofline": _roofline_hbm(gbs, peaks, kind, "kv_write_kernel", per_launch_bytes=nbytes),
+            "roofline": _roofline_hbm(gbs, peaks, kind, "kv_write_kernel", traffic=WRITE_CHUNK_DRAM_BYTES,
+                                      per_launch_bytes=nbytes),
             "gpu_launches": launches, "clocks": clk}
     print(json.dumps(line))
     return 0
@@ -702,7 +715,7 @@ def run_write(args):
 # ------------------------------------------------------------------------------------------------
 
 def _timed_fused_decode(pa, lib, *, lens, Hq, Hkv, Dh, S, dtype, code, pools_count, num_blocks, max_blocks, reps,
-                        warmup, seed, flush_bytes, graph=False, back_to_back=False):
+                        warmup, seed, flush_bytes, graph=False, back_to_back=False, partition_tokens=0):
     """Device time of one paged_attention_decode_fused call.  Per-call: the median of CUDA events around
     single calls that rotate through ``pools_count`` independent pools, with an L2 flush (a write
     of ``flush_bytes``, then a read of as many) before each call when that is non-zero.  ``back_to_back``: also the time per
@@ -720,18 +733,20 @@ def _timed_fused_decode(pa, lib, *, lens, Hq, Hkv, Dh, S, dtype, code, pools_cou
     q, kn, vn = inp["q"].to(dev), inp["k_new"].to(dev), inp["v_new"].to(dev)
     out = torch.empty_like(q)
     B = len(lens)
-    ws_bytes = pa.decode_workspace_size(B, table.stride(0), S, Hq, Hkv, Dh)
+    ws_bytes = pa.decode_workspace_size(B, table.stride(0), S, Hq, Hkv, Dh, partition_tokens=partition_tokens)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = L2Flush(dev, flush_bytes) if flush_bytes else None
+    opts = pa.make_opts(partition_tokens=partition_tokens)
+    optp = ctypes.byref(opts)
     scale = 1.0 / math.sqrt(Dh)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def call(i, s=sp):
         kp, vp = inp["pools"][i % pools_count]
-        st = lib.paged_attention_decode_fused(out.data_ptr(), q.data_ptr(), kn.data_ptr(), vn.data_ptr(),
-                                              slot.data_ptr(), kp.data_ptr(), vp.data_ptr(), table.data_ptr(),
-                                              table.stride(0), ctx.data_ptr(), B, num_blocks, S, scale, Hq, Hkv, Dh,
-                                              code, ws.data_ptr(), ws_bytes, s)
+        st = lib.paged_attention_decode_fused_ex(out.data_ptr(), q.data_ptr(), kn.data_ptr(), vn.data_ptr(),
+                                                 slot.data_ptr(), kp.data_ptr(), vp.data_ptr(), table.data_ptr(),
+                                                 table.stride(0), ctx.data_ptr(), B, num_blocks, S, scale, Hq, Hkv,
+                                                 Dh, code, ws.data_ptr(), ws_bytes, optp, s)
         if st:
             raise RuntimeError(f"paged_attention_decode_fused status {st}")
 
@@ -795,7 +810,8 @@ def run_long(args):
     launches0 = pa.launch_count()
     r = _timed_fused_decode(pa, lib, lens=lens, Hq=HQ, Hkv=HKV, Dh=D, S=S, dtype=torch.bfloat16, code=pa.PA_BF16,
                             pools_count=2, num_blocks=nb, max_blocks=W.ceil_div(max(lens), S), reps=args.steps,
-                            warmup=args.warmup, seed=SEED_LONG, flush_bytes=0, back_to_back=True)
+                            warmup=args.warmup, seed=SEED_LONG, flush_bytes=0, back_to_back=True,
+                            partition_tokens=args.partition_tokens)
     clocks.mark("end")
     clk = clocks.stop()
     launches = pa.launch_count() - launches0
@@ -849,7 +865,8 @@ def run_gpt2(args):
                                     code=pa.PA_FP16, pools_count=W.GPT2_LAYERS,
                                     num_blocks=W.ceil_div(5 * need, 4), max_blocks=W.ceil_div(context, 16),
                                     reps=args.steps, warmup=args.warmup, seed=W.SEED_BASE + 2 + 31 * bi + ci,
-                                    flush_bytes=2 * l2, graph=True, back_to_back=True)
+                                    flush_bytes=2 * l2, graph=True, back_to_back=True,
+                                    partition_tokens=args.partition_tokens)
             kv = batch * context * 12 * 64 * 2 * 2
             qo = 2 * batch * 12 * 64 * 2
             wb = batch * 12 * 64 * 2 * 2 * 2
@@ -879,6 +896,8 @@ def run_gpt2(args):
         "roofline": _roofline_hbm(big["GB/s"], peaks, kind,
                                   f"paged_attention_decode_fused at batch {big['batch']} x {big['context']} "
                                   f"({big['bytes'] / 1e6:.1f} MB per call)",
+                                  traffic=(GPT2_8X2048_DRAM_BYTES if (big["batch"], big["context"]) == (8, 2048)
+                                           and not args.partition_tokens else None),
                                   per_launch_bytes=big["bytes"]),
         "gpu_launches": launches, "clocks": clk,
     }
