@@ -72,6 +72,47 @@ def test_prefill_ragged_chunks(cuda_lib, dtype, D, G, S, kernel):
     assert pa.device_error_flags() == 0
 
 
+def _peak_keys(case, offsets, factor):
+    """Scale the keys of context positions p with p % 128 in ``offsets`` (history keys in the pool,
+    chunk keys in k_new) by ``factor``, in place."""
+    S = case.block_size
+    qsl = case.query_start_loc.tolist()
+    lens = case.context_lens.tolist()
+    for b, n in enumerate(lens):
+        m = qsl[b + 1] - qsl[b]
+        for p in range(n):
+            if p % 128 not in offsets:
+                continue
+            if p < n - m:
+                blk = int(case.block_table[b, p // S])
+                case.k_pool[blk, p % S] = (case.k_pool[blk, p % S].float() * factor).to(case.dtype)
+            else:
+                r = qsl[b] + p - (n - m)
+                case.k_new[r] = (case.k_new[r].float() * factor).to(case.dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("G,D", [(4, 128), (2, 64)])
+def test_prefill_peaked_keys_in_second_half_of_tiles(cuda_lib, dtype, G, D):
+    """Keys in the second 64 keys of 128-key tiles scaled x16: within a tile the scores of keys
+    64..127 exceed those of keys 0..63 by far more than 2^8 in the exponent's base-2 units, so the
+    softmax moves its stabilising maximum after the first half's probabilities are already stored
+    (and, at other rows and tiles, before); every output against the oracle."""
+    pa = cuda_lib
+    case = W.varlen_prefill(77 + G + D, hist_lens=[300, 0, 190, 520], chunk_lens=[96, 200, 33, 128],
+                            block_size=16, n_q_heads=2 * G, n_kv_heads=2, head_dim=D, dtype=dtype,
+                            num_blocks=160)
+    _peak_keys(case, {71, 100, 127}, 16.0)
+    out, _, _ = run_case(pa, case, kernel=0)
+    kp, vp = oracle_pools(case)
+    res = oracle.paged_prefill(case.q, case.query_start_loc, kp, vp, case.block_table, case.context_lens,
+                               case.scale)
+    idx = sorted(res)
+    assert len(idx) == case.q.shape[0]
+    assert_close(out[idx], np.stack([res[i] for i in idx]), dtype, f"peaked {dtype} G{G} D{D}")
+    assert pa.device_error_flags() == 0
+
+
 @pytest.mark.parametrize("G,D", [(4, 128), (8, 64)])
 def test_prefill_many_items_per_cta(cuda_lib, G, D):
     """More (64-token query block, KV head) items than SMs, so every CTA of the tcgen05 kernel
