@@ -65,18 +65,6 @@ constexpr int kUmItemSlots = 4;  // item tile counts in flight between the K pro
 constexpr int kUmKStages = PA_UM_KSTAGES;   // K ring depth
 constexpr int kUmVStages = PA_UM_VSTAGES;   // V ring depth
 constexpr float kUmRescaleThreshold = 8.f;  // log2 units: O is rescaled when the max grows by > 2^8
-// 1: one CTA per SM walking the work items; 0: one CTA per work item
-#ifndef PA_UM_PERSISTENT
-#define PA_UM_PERSISTENT 1
-#endif
-constexpr bool kUmPersistent = PA_UM_PERSISTENT != 0;
-// 0: S_k of the next tile is issued right after O_k += P_k V of this tile (tcgen05.mma products of
-// one thread run in issue order, so the P V reads P_k before the next S_k overwrites its columns);
-// 1: only once that P V has completed (measured 4 % slower)
-#ifndef PA_UM_S_AFTER_PV_DONE
-#define PA_UM_S_AFTER_PV_DONE 0
-#endif
-constexpr bool kUmSAfterPvDone = PA_UM_S_AFTER_PV_DONE != 0;
 
 template <int D>
 struct UmCfg {
@@ -698,11 +686,9 @@ __global__ void __launch_bounds__(kUmThreads)
         for (int j = 0; j < n_all && ok; ++j) {
           const int gj = g + j;
           if (!wait(&kfull[gj % kUmKStages], (unsigned)((gj / kUmKStages) & 1))) break;
-          if (kUmSAfterPvDone && gj > 0 && !wait(&pv_done[0], (unsigned)((gj - 1) & 1))) break;
           tc_fence_after();
           issue_s(0, gj);
           if (j > 0 && !pv_of(1, j - 1)) break;
-          if (kUmSAfterPvDone && gj > 0 && !wait(&pv_done[1], (unsigned)((gj - 1) & 1))) break;
           tc_fence_after();
           issue_s(1, gj);
           umma_commit(&kempty[gj % kUmKStages]);
@@ -904,7 +890,7 @@ static cudaError_t launch_um_g(const AttnArgs& a, const CUtensorMap& km, const C
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) sm_count[dev] = sms;
   }
-  const int64_t grid = kUmPersistent ? std::min<int64_t>(items, sms) : items;
+  const int64_t grid = std::min<int64_t>(items, sms);
   prefill_umma_kernel<T, D, G><<<(unsigned)grid, kUmThreads, smem, s>>>(a, km, vm, qm);
   return cudaGetLastError();
 }
