@@ -8,21 +8,25 @@
 // Persistent: one CTA per SM walks the work items (blockIdx, blockIdx + gridDim, ...).  An item =
 // 256 (query token, head) rows of one KV head, split into two 128-row Q tiles that share every K/V
 // tile (kRows / G tokens x the G heads of the group: read-time GQA, nanoserve Day 19 "What I
-// learned" 4).  11 warps:
+// learned" 4).  11 warps; the producers and the MMA warp run on lane 0 alone (a warp whose lanes
+// meet at warp-collective steps between long single-lane stretches loses about a thousand cycles
+// per meeting):
 //   warps 0-3 / 4-7  softmax groups 0 / 1: thread t of group k owns row 128k + t (TMEM lane t of
-//              S_k and O_k); turns each S_k tile into probabilities, rescales O_k in TMEM only when
-//              its stabilising maximum has to move up by more than 2^8, writes P_k (bf16/fp16) back
-//              into the TMEM columns of S_k, and normalises O_k at the end;
-//   warp 8     K producer: finds each item's segments (the rows of one sequence: a binary search
-//              over query_start_loc and the length loads, dependent global loads that only this
-//              warp waits for, ahead of the others) and publishes the item's tile count (for the
-//              MMA warp) and a record per segment (for the V producer and the softmax groups)
-//              through small shared-memory rings; streams 128-key K tiles (TMA boxes of 16 keys x
-//              64 columns from the physical blocks the table names) into a kUmKStages-deep ring and
-//              publishes which sub-tiles hold data;
+//              S_k and O_k); turns each S_k tile into probabilities (compact code: 64-key blocks
+//              in a loop; one instantiation per masking mode, see ScoreFix), rescales O_k in TMEM
+//              only when its stabilising maximum has to move up by more than 2^8, writes P_k
+//              (bf16/fp16) back into the TMEM columns of S_k, and normalises O_k at the end;
+//   warp 8     K producer: finds each item's segments (the rows of one sequence: an 8-way search
+//              over query_start_loc, then the sequence's bounds and length; for the next item this
+//              runs one step per K tile of the current one, so that its dependent loads overlap
+//              useful waiting) and publishes the item's tile count (for the MMA warp) and a record
+//              per segment (for the V producer and the softmax groups) through small shared-memory
+//              rings; streams 128-key K tiles (TMA boxes of 16 keys x 64 columns from the physical
+//              blocks the table names, the table entries read one tile ahead) into a
+//              kUmKStages-deep ring and publishes which sub-tiles hold data;
 //   warp 9     V producer: each item's two Q tiles (one TMA box per 64-column half, once the
-//              previous item's S products are done), then the matching V tiles into a
-//              kUmVStages-deep ring;
+//              previous item's S products are done; the next item's Q tiles are prefetched into
+//              L2 meanwhile), then the matching V tiles into a kUmVStages-deep ring;
 //   warp 10    MMA: allocates TMEM (S_0, S_1: 128 columns each; O_0, O_1: 128 columns each) and
 //              issues S_k = Q_k K^T (M 128, N 128, both operands in shared memory) and
 //              O_k += P_k V (M 128, N head_dim, P read from TMEM, V an MN-major shared-memory
