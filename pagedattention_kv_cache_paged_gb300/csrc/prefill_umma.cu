@@ -124,10 +124,10 @@ struct ScoreFix {
 // with a separate masked variant, measured slower from instruction fetch alone.
 
 // Columns [c0, c0 + 64) of the row of S into registers (two loads in flight, one wait), rewritten
-// as `fix` says; m0 / m1 are the mask words of the block's two 32-key chunks.  kGeneral = false
-// serves modes 0 and 1 with one copy of the code (the prefix cut is a short block behind a
-// warp-uniform branch, so a masked tile runs the instructions the unmasked ones keep in the
-// instruction cache); kGeneral = true is the rare mode 2.
+// as `fix` says; m0 / m1 are the mask words of the block's two 32-key chunks.  One instantiation
+// per masking mode (kMode = fix.mode): mode 0 runs no masking code at all, mode 1 applies the prefix
+// cut only in a block that the cut falls in, mode 2 is the rare general rewrite.  (One copy of the
+// code for modes 0 and 1, the cut behind a warp-uniform branch, measured slower.)
 template <int kMode>
 __device__ __forceinline__ void s_load64(uint32_t taddr, uint32_t (&sv)[64], const ScoreFix& fix, int c0,
                                          uint32_t m0, uint32_t m1) {
